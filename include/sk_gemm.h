@@ -1,0 +1,196 @@
+/*
+ * sk_gemm.h — C ABI of the GB300 (sm_103a) persistent / SM-constrained / Stream-K addmm GEMM.
+ *
+ * The library computes   C = A * B (+ bias[n] broadcast over every row m)
+ * with fp32 accumulation, for bf16 operands and for MXFP4 operands (E2M1 codes with one E8M0
+ * scale per 32 consecutive K elements), under four work schedules:
+ *
+ *   SK_MODE_DP          data-parallel: one CTA per BM x BN output tile (the non-persistent
+ *                       "naive" GEMM of flashinfer PR #982 "SM-constraint-GEMM by triton
+ *                       persistent kernel", overview).
+ *   SK_MODE_PERSISTENT  SM-constrained persistent grid: g = min(num_sms, SM count, tiles)
+ *                       CTAs, CTA c takes tiles c, c+g, ... (same page: the grid is capped at
+ *                       num_sms, and at the device's SM count — its nsys block shows a request
+ *                       of 133 launched as 132 CTAs).
+ *   SK_MODE_STREAMK     Stream-K: the tiles x k-iterations are split evenly over g CTAs; a CTA
+ *                       whose range starts inside a tile spills its fp32 partial tile to a
+ *                       scratch slot P[cta] and releases a flag; the tile's owner (the CTA
+ *                       holding k = 0) acquires the flags, adds the partials, and only then
+ *                       adds the bias along N and stores (tritonBLAS PR #67 "Fix StreamK Kernel
+ *                       Bias", Motivation and Technical Details; tritonBLAS PR #74 "Stream-k
+ *                       mxfp4 kernel": one P slot and one lock per CTA).
+ *   SK_MODE_HYBRID      the last (tiles mod g) tiles run Stream-K over all g CTAs (each CTA does
+ *                       its Stream-K share first), the other tiles run whole, round-robin.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers A, B, bias, C, A_scale, B_scale are DEVICE pointers owned by the caller, on the
+ *     current CUDA device; they must stay valid until the work queued on `stream` has run.
+ *     Each must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   - Calls are asynchronous: the return value reports argument checks and enqueue errors
+ *     only.  Errors found by the kernel (a Stream-K wait that timed out) are recorded in the
+ *     stream's workspace and returned by sk_stream_status().
+ *   - No exception crosses this boundary; every failure is a status code.
+ *   - Scratch (the Stream-K partial slots P, their flags, the error words and the MXFP4
+ *     scale-layout buffers) belongs to the library: one workspace per (device, stream), created
+ *     on first use and grown on demand, never at load time and never on a default device.
+ *     While `stream` is being captured into a CUDA graph no allocation is made; a workspace too
+ *     small for the call then yields SK_ERR_UNSUPPORTED (reserve it beforehand with
+ *     sk_workspace_reserve()).
+ *   - Calls on one stream are ordered.  Calls on different streams use different workspaces
+ *     and may run concurrently.
+ */
+#ifndef SK_GEMM_H
+#define SK_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SK_MODE_DP = 0,
+  SK_MODE_PERSISTENT = 1,
+  SK_MODE_STREAMK = 2,
+  SK_MODE_HYBRID = 3
+} sk_mode_t;
+
+/* dtype of C, and of bias (the bias always has C's dtype) */
+typedef enum { SK_F32 = 0, SK_BF16 = 1 } sk_dtype_t;
+
+typedef enum {
+  SK_OK = 0,
+  SK_ERR_INVALID_ARG = 1,     /* bad size, null or misaligned pointer, bad enum value      */
+  SK_ERR_UNSUPPORTED = 2,     /* valid request this build cannot run (e.g. no sm_103 GPU,  */
+                              /* or workspace too small while the stream is capturing)     */
+  SK_ERR_OOM = 3,             /* workspace allocation failed                               */
+  SK_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed                         */
+  SK_ERR_TIMEOUT = 5,         /* kernel-side: a bounded wait ran out (see sk_stream_status) */
+  SK_ERR_NOT_CORESIDENT = 6   /* Stream-K/hybrid grid cannot be fully resident at once     */
+} sk_status_t;
+
+/*
+ * sk_gemm_bf16 — C[M x N] = A[M x K] * B[K x N] (+ bias[N]).
+ *   A: bf16, row-major M x K (row pitch K elements).  K must be a multiple of 8.
+ *   B: bf16, row-major K x N (the torch `mm(a, b)` layout; row pitch N).  N must be a
+ *      multiple of 8 (16-byte row pitch for the tensor-memory-accelerator loads).
+ *   bias: NULL, or N values of out_dtype.  Added once per output element, after all partial
+ *      tiles are summed, broadcast over rows (tritonBLAS PR #67, Technical Details).
+ *   C: row-major M x N of out_dtype (SK_BF16: rounded to nearest-even from fp32; SK_F32).
+ *   M, N, K >= 1 and < 2^31.
+ *   num_sms: <= 0 means every SM; larger than the SM count is capped to it.  Ignored by
+ *      SK_MODE_DP (grid = number of tiles).
+ * Returns SK_OK once the kernel is queued on `stream`.
+ */
+sk_status_t sk_gemm_bf16(const void* A, const void* B, const void* bias, void* C,
+                         sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
+                         sk_mode_t mode, void* stream);
+
+/*
+ * sk_gemm_mxfp4 — the same product for MXFP4 operands (tritonBLAS PR #74 "Stream-k mxfp4
+ * kernel"; encoding per OCP MX v1.0).
+ *   A:       uint8, M x K/2 bytes, two E2M1 codes per byte packed along K, the even-k element
+ *            in the low nibble.
+ *   A_scale: uint8 E8M0, M x K/32, row-major; byte (m, j) scales A[m][32j .. 32j+31] by
+ *            2^(E-127) (E = 255 is NaN and propagates).
+ *   B:       uint8, N x K/2 bytes (B stored transposed: row n holds column n of the K x N
+ *            operand, packed along K like A).
+ *   B_scale: uint8 E8M0, N x K/32.
+ *   K must be a multiple of 32.  M, N >= 1 (any value).  Other arguments as sk_gemm_bf16.
+ * The call also runs a small kernel that rearranges the two scale arrays into the order the
+ * tensor cores read them (into the stream's workspace); it is part of every call.
+ */
+sk_status_t sk_gemm_mxfp4(const void* A, const void* A_scale, const void* B,
+                          const void* B_scale, const void* bias, void* C, sk_dtype_t out_dtype,
+                          int64_t M, int64_t N, int64_t K, int num_sms, sk_mode_t mode,
+                          void* stream);
+
+/*
+ * Optional tuning and test controls for the *_ex entry points.  Zero-initialise, then set
+ * fields; a NULL options pointer means all defaults.
+ *   tile_n:               0 = automatic, else 128 or 256 (columns per CTA tile; MXFP4 only 128).
+ *   raster_group:         0 = automatic, else rows of tiles per group in the tile order.
+ *   spin_timeout_ns:      0 = default (2 s).  Bound on every wait inside the kernel; when it
+ *                         runs out the kernel records SK_ERR_TIMEOUT, skips the affected
+ *                         stores and returns normally.
+ *   drop_release_cta:     fault injection for tests, -1 (or any value when zeroed options are
+ *                         passed with inject_faults = 0) = off.  When inject_faults != 0, the
+ *                         CTA with this index never releases its Stream-K partial, so its
+ *                         tile's owner times out.
+ */
+typedef struct {
+  int32_t tile_n;
+  int32_t raster_group;
+  int64_t spin_timeout_ns;
+  int32_t inject_faults;
+  int32_t drop_release_cta;
+} sk_options_t;
+
+sk_status_t sk_gemm_bf16_ex(const void* A, const void* B, const void* bias, void* C,
+                            sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
+                            sk_mode_t mode, const sk_options_t* options, void* stream);
+
+sk_status_t sk_gemm_mxfp4_ex(const void* A, const void* A_scale, const void* B,
+                             const void* B_scale, const void* bias, void* C,
+                             sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
+                             sk_mode_t mode, const sk_options_t* options, void* stream);
+
+/*
+ * sk_stream_status — waits for `stream`, then returns (and clears) the first error the kernels
+ * recorded in that stream's workspace on the current device: SK_OK, SK_ERR_TIMEOUT, or
+ * SK_ERR_CUDA if the stream itself reports a CUDA error.
+ */
+sk_status_t sk_stream_status(void* stream);
+
+/*
+ * sk_workspace_reserve — size the workspace of (device, stream) for grids of up to max_grid
+ * CTAs and MXFP4 problems of up to max_mx_m x max_mx_n x max_mx_k (0 = none), so that later
+ * calls (e.g. while the stream is captured into a CUDA graph) need no allocation.
+ */
+sk_status_t sk_workspace_reserve(int device, void* stream, int max_grid, int64_t max_mx_m,
+                                 int64_t max_mx_n, int64_t max_mx_k);
+
+/* Frees every workspace (synchronises each device that has one first). */
+void sk_workspace_release_all(void);
+
+/* Static English description of a status code. */
+const char* sk_status_string(sk_status_t status);
+
+/*
+ * Planning (host only, makes no CUDA call).  Fills *plan with the schedule the library would
+ * launch for this problem on a device with `sm_count` SMs.  format: 0 = bf16, 1 = MXFP4.
+ */
+typedef struct {
+  int32_t format;
+  int32_t mode;
+  int32_t tile_m, tile_n, tile_k;   /* CTA tile; tile_k in elements per k-iteration       */
+  int32_t tiles_m, tiles_n;
+  int64_t tiles;                    /* tiles_m * tiles_n                                  */
+  int32_t iters;                    /* k-iterations per tile                              */
+  int32_t grid;                     /* CTAs launched                                      */
+  int32_t raster_group;
+  int32_t reserved;
+  int64_t whole_tiles;              /* linear tiles [0, whole_tiles) run whole            */
+  int64_t sk_tiles;                 /* linear tiles [whole_tiles, tiles) run Stream-K     */
+  int64_t sk_base;                  /* Stream-K iterations per CTA ...                    */
+  int64_t sk_extra;                 /* ... plus one for CTAs [0, sk_extra)                */
+} sk_plan_t;
+
+sk_status_t sk_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, sk_mode_t mode,
+                    int sm_count, const sk_options_t* options, sk_plan_t* plan);
+
+/*
+ * Enumerates the work the kernel's CTAs perform for `plan`, in each CTA's execution order:
+ * rows of 7 int64 (cta, linear tile, k_begin, k_end, role, tile_m index, tile_n index), role
+ * 0 = whole tile, 1 = owner of a split tile, 2 = partial contribution.  Writes at most `cap`
+ * rows and returns the total count (call with cap = 0 to size the buffer), or -1 on bad input.
+ * This runs the same scheduling code the kernel runs.
+ */
+int64_t sk_plan_segments(const sk_plan_t* plan, int64_t* rows, int64_t cap);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SK_GEMM_H */

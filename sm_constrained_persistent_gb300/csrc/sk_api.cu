@@ -1,0 +1,498 @@
+// C-ABI layer: argument checks, schedule planning, per-(device, stream) workspaces, TMA
+// descriptor encoding and kernel launches.  Declared in include/sk_gemm.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "sk_gemm.h"
+#include "sk_launch.h"
+#include "sk_schedule.cuh"
+
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kBf16TileK = 64;
+constexpr int kMxTileK = 256;
+constexpr int kDefaultRasterGroup = 16;
+constexpr int64_t kDefaultTimeoutNs = 2000000000LL;   // 2 s
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+// ---------------------------------------------------------------------------------------
+// planning (pure host arithmetic)
+// ---------------------------------------------------------------------------------------
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+sk_status_t make_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, int mode,
+                      int sm_count, const sk_options_t* opt, sk_plan_t* p) {
+  if (p == nullptr || (format != 0 && format != 1) || mode < 0 || mode > 3 || sm_count < 1)
+    return SK_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return SK_ERR_INVALID_ARG;
+  int tile_n = opt ? opt->tile_n : 0;
+  if (tile_n != 0 && tile_n != 128 && tile_n != 256) return SK_ERR_INVALID_ARG;
+  if (format == 1 && tile_n == 256) return SK_ERR_INVALID_ARG;
+  if (tile_n == 0) {
+    if (format == 1) {
+      tile_n = 128;
+    } else {
+      // Wide tiles halve the B traffic per FLOP; use them while they still fill every SM.
+      const int64_t wide_tiles = ceil_div(M, kTileM) * ceil_div(N, 256);
+      tile_n = (N >= 256 && wide_tiles >= sm_count) ? 256 : 128;
+    }
+  }
+  std::memset(p, 0, sizeof(*p));
+  p->format = format;
+  p->mode = mode;
+  p->tile_m = kTileM;
+  p->tile_n = tile_n;
+  p->tile_k = format == 1 ? kMxTileK : kBf16TileK;
+  const int64_t tiles_m = ceil_div(M, kTileM), tiles_n = ceil_div(N, tile_n);
+  const int64_t tiles = tiles_m * tiles_n;
+  const int64_t iters = ceil_div(K, p->tile_k);
+  if (tiles > kMaxDim) return SK_ERR_UNSUPPORTED;
+  p->tiles_m = static_cast<int32_t>(tiles_m);
+  p->tiles_n = static_cast<int32_t>(tiles_n);
+  p->tiles = tiles;
+  p->iters = static_cast<int32_t>(iters);
+  const int64_t sms = (num_sms <= 0 || num_sms > sm_count) ? sm_count : num_sms;
+  int64_t grid = 0, sk_tiles = 0;
+  switch (mode) {
+    case SK_MODE_DP: grid = tiles; sk_tiles = 0; break;
+    case SK_MODE_PERSISTENT: grid = std::min(sms, tiles); sk_tiles = 0; break;
+    case SK_MODE_STREAMK: grid = std::min(sms, tiles * iters); sk_tiles = tiles; break;
+    default: grid = std::min(sms, tiles * iters); sk_tiles = tiles % grid; break;
+  }
+  p->grid = static_cast<int32_t>(grid);
+  p->whole_tiles = tiles - sk_tiles;
+  p->sk_tiles = sk_tiles;
+  p->sk_base = sk_tiles * iters / grid;
+  p->sk_extra = sk_tiles * iters % grid;
+  int group = opt && opt->raster_group > 0 ? opt->raster_group : kDefaultRasterGroup;
+  p->raster_group = static_cast<int32_t>(std::min<int64_t>(group, tiles_m));
+  return SK_OK;
+}
+
+sk::Plan kernel_plan(const sk_plan_t& p) {
+  sk::Plan k = {};
+  k.tiles_m = p.tiles_m;
+  k.tiles_n = p.tiles_n;
+  k.iters = p.iters;
+  k.grid = p.grid;
+  k.group_m = p.raster_group;
+  k.tiles = p.tiles;
+  k.whole_tiles = p.whole_tiles;
+  k.sk_base = p.sk_base;
+  k.sk_extra = p.sk_extra;
+  return k;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// ---------------------------------------------------------------------------------------
+// devices, workspaces, tensor maps
+// ---------------------------------------------------------------------------------------
+
+struct DeviceInfo {
+  bool known = false;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  bool variant_ready[sk::kNumVariants] = {};
+  int ctas_per_sm[sk::kNumVariants] = {};
+};
+
+struct Workspace {
+  float* P = nullptr;
+  size_t P_bytes = 0;
+  uint32_t* flags = nullptr;
+  size_t flag_count = 0;
+  uint32_t* err = nullptr;     // 4 words
+  uint8_t* sf = nullptr;
+  size_t sf_bytes = 0;
+  uint32_t epoch = 0;
+};
+
+std::mutex g_mutex;
+std::map<int, DeviceInfo> g_devices;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D tensor map over a row-major matrix [rows][cols] of `elem` bytes per element, boxes of
+// box_cols x box_rows elements, 128-byte swizzle, zero fill outside the matrix.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, size_t elem, const void* base,
+               int64_t rows, int64_t cols, uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Caller holds g_mutex.
+sk_status_t device_info(int dev, DeviceInfo** out) {
+  DeviceInfo& d = g_devices[dev];
+  if (!d.known) {
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return SK_ERR_CUDA;
+    d.known = true;
+  }
+  *out = &d;
+  return SK_OK;
+}
+
+sk_status_t ensure_variant(DeviceInfo& d, int variant) {
+  if (!d.variant_ready[variant]) {
+    int n = 0;
+    if (sk::variant_setup(variant, &n) != cudaSuccess) return SK_ERR_CUDA;
+    d.ctas_per_sm[variant] = n;
+    d.variant_ready[variant] = true;
+  }
+  return SK_OK;
+}
+
+template <class T>
+cudaError_t regrow(T** ptr, size_t* have, size_t need, cudaStream_t st) {
+  if (*have >= need && *ptr != nullptr) return cudaSuccess;
+  if (*ptr != nullptr) {
+    cudaError_t e = cudaFreeAsync(*ptr, st);
+    if (e != cudaSuccess) return e;
+    *ptr = nullptr;
+    *have = 0;
+  }
+  void* p = nullptr;
+  cudaError_t e = cudaMallocAsync(&p, need, st);
+  if (e != cudaSuccess) return e;
+  *ptr = static_cast<T*>(p);
+  *have = need;
+  return cudaSuccess;
+}
+
+// Caller holds g_mutex.  Grows the workspace of (dev, st) to at least the given sizes.
+sk_status_t ensure_workspace(int dev, cudaStream_t st, size_t P_bytes, size_t flag_count,
+                             size_t sf_bytes, Workspace** out) {
+  Workspace& w = g_workspaces[{dev, st}];
+  const bool fits = w.err != nullptr && w.P_bytes >= P_bytes && w.flag_count >= flag_count &&
+                    w.sf_bytes >= sf_bytes;
+  if (!fits) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return SK_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return SK_ERR_UNSUPPORTED;
+    if (w.err == nullptr) {
+      size_t have = 0;
+      if (regrow(&w.err, &have, 16, st) != cudaSuccess) return SK_ERR_OOM;
+      if (cudaMemsetAsync(w.err, 0, 16, st) != cudaSuccess) return SK_ERR_CUDA;
+    }
+    if (P_bytes > 0 && regrow(&w.P, &w.P_bytes, P_bytes, st) != cudaSuccess) return SK_ERR_OOM;
+    if (w.flag_count < flag_count || w.flags == nullptr) {
+      size_t bytes = w.flag_count * sizeof(uint32_t);
+      const size_t need = std::max<size_t>(flag_count, 1) * sizeof(uint32_t);
+      if (regrow(&w.flags, &bytes, need, st) != cudaSuccess) return SK_ERR_OOM;
+      w.flag_count = bytes / sizeof(uint32_t);
+      if (cudaMemsetAsync(w.flags, 0, bytes, st) != cudaSuccess) return SK_ERR_CUDA;
+    }
+    if (sf_bytes > 0 && regrow(&w.sf, &w.sf_bytes, sf_bytes, st) != cudaSuccess) return SK_ERR_OOM;
+  }
+  *out = &w;
+  return SK_OK;
+}
+
+struct MxLayout {
+  int64_t kgroups, a_row_blocks, b_row_blocks;
+  size_t bytes() const { return static_cast<size_t>((a_row_blocks + b_row_blocks) * kgroups * 512); }
+};
+
+MxLayout mx_layout(const sk_plan_t& p) {
+  MxLayout l;
+  l.kgroups = 2 * static_cast<int64_t>(p.iters);
+  l.a_row_blocks = p.tiles_m;
+  l.b_row_blocks = static_cast<int64_t>(p.tiles_n) * (p.tile_n / 128);
+  return l;
+}
+
+// ---------------------------------------------------------------------------------------
+// the GEMM call
+// ---------------------------------------------------------------------------------------
+
+sk_status_t validate(int format, const void* A, const void* A_scale, const void* B,
+                     const void* B_scale, const void* bias, const void* C, int out_dtype,
+                     int64_t M, int64_t N, int64_t K, int mode, const sk_options_t* opt) {
+  if (A == nullptr || B == nullptr || C == nullptr) return SK_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (bias && !aligned16(bias)))
+    return SK_ERR_INVALID_ARG;
+  if (out_dtype != SK_F32 && out_dtype != SK_BF16) return SK_ERR_INVALID_ARG;
+  if (mode < SK_MODE_DP || mode > SK_MODE_HYBRID) return SK_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return SK_ERR_INVALID_ARG;
+  if (format == 0) {
+    if (K % 8 != 0 || N % 8 != 0) return SK_ERR_INVALID_ARG;   // 16-byte row pitches
+  } else {
+    if (A_scale == nullptr || B_scale == nullptr) return SK_ERR_INVALID_ARG;
+    if (K % 32 != 0) return SK_ERR_INVALID_ARG;
+  }
+  if (opt != nullptr) {
+    if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256) return SK_ERR_INVALID_ARG;
+    if (format == 1 && opt->tile_n == 256) return SK_ERR_INVALID_ARG;
+    if (opt->spin_timeout_ns < 0 || opt->raster_group < 0) return SK_ERR_INVALID_ARG;
+  }
+  return SK_OK;
+}
+
+sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void* B,
+                     const void* B_scale, const void* bias, void* C, sk_dtype_t out_dtype,
+                     int64_t M, int64_t N, int64_t K, int num_sms, sk_mode_t mode,
+                     const sk_options_t* opt, void* stream_ptr) {
+  sk_status_t st = validate(format, A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, mode, opt);
+  if (st != SK_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SK_ERR_UNSUPPORTED;
+
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(dev, &di)) != SK_OK) return st;
+  if (di->cc_major != 10 || di->cc_minor != 3) return SK_ERR_UNSUPPORTED;   // built for sm_103a
+
+  sk_plan_t plan;
+  if ((st = make_plan(format, M, N, K, num_sms, mode, di->sm_count, opt, &plan)) != SK_OK) return st;
+  const int variant = format == 1 ? sk::kVariantMxN128
+                                  : (plan.tile_n == 256 ? sk::kVariantBf16N256 : sk::kVariantBf16N128);
+  if ((st = ensure_variant(*di, variant)) != SK_OK) return st;
+  const bool streamk = plan.sk_tiles > 0;
+  if (streamk && static_cast<int64_t>(plan.grid) >
+                     static_cast<int64_t>(di->ctas_per_sm[variant]) * di->sm_count)
+    return SK_ERR_NOT_CORESIDENT;
+
+  const size_t P_bytes = streamk ? static_cast<size_t>(plan.grid) * kTileM * plan.tile_n * sizeof(float) : 0;
+  const MxLayout mx = mx_layout(plan);
+  Workspace* ws = nullptr;
+  if ((st = ensure_workspace(dev, stream, P_bytes, static_cast<size_t>(plan.grid),
+                             format == 1 ? mx.bytes() : 0, &ws)) != SK_OK)
+    return st;
+  if (++ws->epoch == 0) ws->epoch = 1;
+
+  CUtensorMap tmA, tmB;
+  bool ok;
+  if (format == 0) {
+    ok = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, M, K, 64, kTileM) &&
+         encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, 64, 64);
+  } else {
+    ok = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, M, K / 2, 128, kTileM) &&
+         encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, N, K / 2, 128,
+                   static_cast<uint32_t>(plan.tile_n));
+  }
+  if (!ok) return SK_ERR_CUDA;
+
+  sk::Launch l = {};
+  l.tmA = &tmA;
+  l.tmB = &tmB;
+  l.grid = plan.grid;
+  l.cooperative = streamk;
+  l.stream = stream;
+  sk::Args& a = l.args;
+  a.bias = bias;
+  a.C = C;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.out_bf16 = out_dtype == SK_BF16 ? 1 : 0;
+  a.inject_drop = (opt != nullptr && opt->inject_faults) ? 1 : 0;
+  a.drop_cta = opt != nullptr ? opt->drop_release_cta : -1;
+  a.epoch = ws->epoch;
+  a.plan = kernel_plan(plan);
+  a.P = ws->P;
+  a.flags = ws->flags;
+  a.err = ws->err;
+  a.timeout_ns = static_cast<uint64_t>(
+      opt != nullptr && opt->spin_timeout_ns > 0 ? opt->spin_timeout_ns : kDefaultTimeoutNs);
+  if (format == 1) {
+    uint8_t* sfa = ws->sf;
+    uint8_t* sfb = ws->sf + mx.a_row_blocks * mx.kgroups * 512;
+    if (sk::mx_scale_prep(static_cast<const uint8_t*>(A_scale), M, K / 32, mx.a_row_blocks,
+                          mx.kgroups, sfa, di->sm_count, stream) != cudaSuccess ||
+        sk::mx_scale_prep(static_cast<const uint8_t*>(B_scale), N, K / 32, mx.b_row_blocks,
+                          mx.kgroups, sfb, di->sm_count, stream) != cudaSuccess)
+      return SK_ERR_CUDA;
+    a.sfa = sfa;
+    a.sfb = sfb;
+    a.sf_kgroups = mx.kgroups;
+  }
+  cudaError_t e = sk::variant_launch(variant, l);
+  if (e == cudaErrorCooperativeLaunchTooLarge) return SK_ERR_NOT_CORESIDENT;
+  return e == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+sk_status_t sk_gemm_bf16(const void* A, const void* B, const void* bias, void* C,
+                         sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
+                         sk_mode_t mode, void* stream) {
+  return run_gemm(0, A, nullptr, B, nullptr, bias, C, out_dtype, M, N, K, num_sms, mode, nullptr,
+                  stream);
+}
+
+sk_status_t sk_gemm_bf16_ex(const void* A, const void* B, const void* bias, void* C,
+                            sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
+                            sk_mode_t mode, const sk_options_t* options, void* stream) {
+  return run_gemm(0, A, nullptr, B, nullptr, bias, C, out_dtype, M, N, K, num_sms, mode, options,
+                  stream);
+}
+
+sk_status_t sk_gemm_mxfp4(const void* A, const void* A_scale, const void* B,
+                          const void* B_scale, const void* bias, void* C, sk_dtype_t out_dtype,
+                          int64_t M, int64_t N, int64_t K, int num_sms, sk_mode_t mode,
+                          void* stream) {
+  return run_gemm(1, A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sms, mode, nullptr,
+                  stream);
+}
+
+sk_status_t sk_gemm_mxfp4_ex(const void* A, const void* A_scale, const void* B,
+                             const void* B_scale, const void* bias, void* C,
+                             sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
+                             sk_mode_t mode, const sk_options_t* options, void* stream) {
+  return run_gemm(1, A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sms, mode, options,
+                  stream);
+}
+
+sk_status_t sk_stream_status(void* stream_ptr) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SK_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SK_ERR_CUDA;
+  uint32_t* err = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto it = g_workspaces.find({dev, stream});
+    if (it == g_workspaces.end() || it->second.err == nullptr) return SK_OK;
+    err = it->second.err;
+  }
+  uint32_t words[4] = {0, 0, 0, 0};
+  if (cudaMemcpyAsync(words, err, sizeof(words), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return SK_ERR_CUDA;
+  if (words[0] == 0) return SK_OK;
+  if (cudaMemsetAsync(err, 0, sizeof(words), stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return SK_ERR_CUDA;
+  return static_cast<sk_status_t>(words[0]);
+}
+
+sk_status_t sk_workspace_reserve(int device, void* stream_ptr, int max_grid, int64_t max_mx_m,
+                                 int64_t max_mx_n, int64_t max_mx_k) {
+  if (max_grid < 1 || max_mx_m < 0 || max_mx_n < 0 || max_mx_k < 0 || (max_mx_k % 32) != 0)
+    return SK_ERR_INVALID_ARG;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return SK_ERR_CUDA;
+  if (cudaSetDevice(device) != cudaSuccess) return SK_ERR_INVALID_ARG;
+  sk_status_t st = SK_OK;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    size_t sf_bytes = 0;
+    if (max_mx_m > 0 && max_mx_n > 0 && max_mx_k > 0) {
+      sk_plan_t p;
+      st = make_plan(1, max_mx_m, max_mx_n, max_mx_k, 0, SK_MODE_DP, 1, nullptr, &p);
+      if (st == SK_OK) sf_bytes = mx_layout(p).bytes();
+    }
+    Workspace* ws = nullptr;
+    if (st == SK_OK)
+      st = ensure_workspace(device, static_cast<cudaStream_t>(stream_ptr),
+                            static_cast<size_t>(max_grid) * kTileM * 256 * sizeof(float),
+                            static_cast<size_t>(max_grid), sf_bytes, &ws);
+  }
+  cudaSetDevice(prev);
+  return st;
+}
+
+void sk_workspace_release_all(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return;
+  for (auto& kv : g_workspaces) {
+    if (cudaSetDevice(kv.first.first) != cudaSuccess) continue;
+    cudaDeviceSynchronize();
+    Workspace& w = kv.second;
+    if (w.P) cudaFree(w.P);
+    if (w.flags) cudaFree(w.flags);
+    if (w.err) cudaFree(w.err);
+    if (w.sf) cudaFree(w.sf);
+  }
+  g_workspaces.clear();
+  cudaSetDevice(prev);
+}
+
+const char* sk_status_string(sk_status_t s) {
+  switch (s) {
+    case SK_OK: return "ok";
+    case SK_ERR_INVALID_ARG: return "invalid argument";
+    case SK_ERR_UNSUPPORTED: return "unsupported request (device or capture state)";
+    case SK_ERR_OOM: return "workspace allocation failed";
+    case SK_ERR_CUDA: return "CUDA call failed";
+    case SK_ERR_TIMEOUT: return "a bounded wait inside the kernel ran out";
+    case SK_ERR_NOT_CORESIDENT: return "Stream-K grid cannot be resident all at once";
+  }
+  return "unknown status";
+}
+
+sk_status_t sk_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, sk_mode_t mode,
+                    int sm_count, const sk_options_t* options, sk_plan_t* plan) {
+  return make_plan(format, M, N, K, num_sms, mode, sm_count, options, plan);
+}
+
+int64_t sk_plan_segments(const sk_plan_t* plan, int64_t* rows, int64_t cap) {
+  if (plan == nullptr || plan->grid < 1 || plan->iters < 1 || plan->tiles < 1) return -1;
+  const sk::Plan p = kernel_plan(*plan);
+  int64_t n = 0;
+  for (int64_t cta = 0; cta < p.grid; ++cta) {
+    sk::Cursor cur(p, cta);
+    sk::Unit u;
+    while (cur.next(p, u)) {
+      if (n < cap && rows != nullptr) {
+        int32_t tm, tn;
+        sk::tile_coords(p, u.tile, tm, tn);
+        int64_t* r = rows + 7 * n;
+        r[0] = cta;
+        r[1] = u.tile;
+        r[2] = u.k0;
+        r[3] = u.k1;
+        r[4] = u.role;
+        r[5] = tm;
+        r[6] = tn;
+      }
+      ++n;
+    }
+  }
+  return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,499 @@
+// The addmm GEMM kernel for sm_103a: C = A * B (+ bias[n]), fp32 accumulation in tensor
+// memory, for bf16 operands (tcgen05 kind::f16) and MXFP4 operands (tcgen05 kind::mxf4 with
+// E8M0 block scales), under the data-parallel, SM-constrained persistent, Stream-K and hybrid
+// schedules of sk_schedule.cuh.
+//
+// One CTA of 192 threads per SM, warp-specialised:
+//   warp 0      TMA producer: streams the A and B tiles of every k-iteration (and the MXFP4
+//               scale blocks) into a ring of shared-memory stages, each guarded by a "full"
+//               mbarrier (transaction bytes) and an "empty" mbarrier (released by the MMAs).
+//   warp 1      allocates tensor memory, then one lane issues the tcgen05 MMAs of each piece
+//               into one of two fp32 accumulators (128 lanes x BN columns each), so the
+//               epilogue of one tile overlaps the main loop of the next.
+//   warps 2..5  epilogue, thread = tile row: tensor memory -> registers, then by role
+//                 whole tile / owner:  (+ partials of the contributors) + bias[n] -> cast ->
+//                                      store C;
+//                 contribution:        fp32 partial -> this CTA's scratch slot P[cta] with
+//                                      coalesced 16-byte stores, then a release of
+//                                      flags[cta].
+// The bias is added only where a tile is finished (whole tile or owner, after all partials),
+// never by a contributor (tritonBLAS PR #67 "Fix StreamK Kernel Bias", Motivation).
+//
+// Every wait is bounded (global timer); when one runs out the kernel records SK_ERR_TIMEOUT
+// in the workspace error words, skips the stores that depend on it, waits (bounded) for its
+// own copies and MMAs in flight, frees its tensor memory and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "sk_kernel_args.h"
+#include "sk_ptx.cuh"
+#include "sk_schedule.cuh"
+
+namespace sk {
+
+constexpr int kBM = 128;          // rows per CTA tile (tcgen05 M = 128, one row per TMEM lane)
+constexpr int kThreads = 192;
+constexpr int kEpilogueThreads = 128;
+constexpr uint32_t kErrTimeout = 5;   // numeric value of SK_ERR_TIMEOUT
+
+// outcome of one piece, as decided by the epilogue's first thread
+enum : uint32_t { kUnitStore = 0, kUnitSkip = 1, kUnitAbort = 2 };
+
+// where a wait ran out (second error word)
+enum : uint32_t {
+  kSiteFlag = 1,
+  kSiteProducer = 2,
+  kSiteMma = 3,
+  kSiteEpilogue = 4,
+  kSiteDrain = 5
+};
+
+
+
+template <bool kMx, int kBN>
+struct Cfg {
+  static_assert(kBN == 128 || kBN == 256, "tile width");
+  static_assert(!kMx || kBN == 128, "MXFP4 tiles are 128 wide");
+  static constexpr int kTileK = kMx ? 256 : 64;        // K elements per k-iteration (128 B rows)
+  static constexpr int kMmaK = kMx ? 64 : 16;          // K per tcgen05.mma
+  static constexpr int kMmasPerStage = kTileK / kMmaK; // 4
+  static constexpr int kStageA = kBM * 128;
+  static constexpr int kStageB = kBN * 128;
+  static constexpr int kStageSfa = kMx ? 1024 : 0;               // 2 k groups x 512 B
+  static constexpr int kStageSfb = kMx ? (kBN / 128) * 1024 : 0;
+  static constexpr int kStages = (192 * 1024) / (kStageA + kStageB);
+  static constexpr int kStageBytes = kStageA + kStageB + kStageSfa + kStageSfb;
+  static constexpr uint32_t kAccCols = kBN;
+  static constexpr uint32_t kSfaCols = 8;              // per stage: 2 groups x 4 columns
+  static constexpr uint32_t kSfbCols = 2 * (kBN / 32); // per stage: 2 groups x BN/32 columns
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(2 * kAccCols + (kMx ? kStages * (kSfaCols + kSfbCols) : 0) <= kTmemCols,
+                "tensor memory budget");
+  static constexpr int kBarrierBytes = 256;
+  static constexpr size_t kSmemBytes =
+      1024 + static_cast<size_t>(kStages) * kStageBytes + kBarrierBytes;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  // Instruction descriptor: fp32 D, K-major A; bf16: bf16 A/B, MN-major B;
+  // MXFP4: E2M1 A/B, E8M0 scales.  N >> 3 at bit 17, M >> 4 at bit 24.
+  static constexpr uint32_t kIdesc =
+      kMx ? ((1u << 7) | (1u << 10) | (1u << 23) | (uint32_t(kBN >> 3) << 17) |
+             (uint32_t(kBM >> 4) << 24))
+          : ((1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | (uint32_t(kBN >> 3) << 17) |
+             (uint32_t(kBM >> 4) << 24));
+};
+
+__device__ __forceinline__ void record_error(const Args& a, uint32_t site, int64_t tile) {
+  if (atomicCAS(&a.err[0], 0u, kErrTimeout) == 0u) {
+    a.err[1] = site;
+    a.err[2] = blockIdx.x;
+    a.err[3] = static_cast<uint32_t>(tile);
+  }
+}
+
+// Bounded mbarrier wait.  Gives up when the CTA has aborted or the time limit runs out (then
+// it records the error and aborts the CTA).
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity,
+                                         volatile uint32_t* abort_flag, const Args& a,
+                                         uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++n & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > a.timeout_ns) {
+        *abort_flag = 1;
+        record_error(a, site, -1);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait used while tearing down: no abort check.
+__device__ __forceinline__ bool wait_bar_drain(uint64_t* bar, uint32_t parity, uint64_t limit) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch,
+                                          uint64_t timeout_ns) {
+  if (flag_acquire(flag) == epoch) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t ns = 32;
+  while (true) {
+    __nanosleep(ns);
+    if (ns < 1024) ns <<= 1;
+    if (flag_acquire(flag) == epoch) return true;
+    if (global_timer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// Adds the bias, casts and stores 32 consecutive columns [n0, n0+32) of row m.
+__device__ __forceinline__ void store_row_chunk(const Args& a, int64_t m, int64_t n0,
+                                                float (&v)[32]) {
+  if (m >= a.M) return;
+  const bool full_chunk = (n0 + 32 <= a.N) && ((a.N & 7) == 0);
+  if (a.out_bf16) {
+    const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(a.bias);
+    __nv_bfloat16* c = static_cast<__nv_bfloat16*>(a.C) + m * a.N + n0;
+    if (full_chunk) {
+      if (bias != nullptr) {
+        const uint4* bp = reinterpret_cast<const uint4*>(bias + n0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 w = __ldg(bp + q);
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float2 f = __bfloat1622float2(h[e]);
+            v[8 * q + 2 * e] += f.x;
+            v[8 * q + 2 * e + 1] += f.y;
+          }
+        }
+      }
+      uint4* cp = reinterpret_cast<uint4*>(c);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+        cp[q] = w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (n0 + j < a.N) {
+          float y = v[j];
+          if (bias != nullptr) y += __bfloat162float(bias[n0 + j]);
+          c[j] = __float2bfloat16_rn(y);
+        }
+      }
+    }
+  } else {
+    const float* bias = static_cast<const float*>(a.bias);
+    float* c = static_cast<float*>(a.C) + m * a.N + n0;
+    if (full_chunk) {
+      if (bias != nullptr) {
+        const float4* bp = reinterpret_cast<const float4*>(bias + n0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float4 f = __ldg(bp + q);
+          v[4 * q] += f.x;
+          v[4 * q + 1] += f.y;
+          v[4 * q + 2] += f.z;
+          v[4 * q + 3] += f.w;
+        }
+      }
+      float4* cp = reinterpret_cast<float4*>(c);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) cp[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (n0 + j < a.N) c[j] = v[j] + (bias != nullptr ? bias[n0 + j] : 0.0f);
+      }
+    }
+  }
+}
+
+template <bool kMx, int kBN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ Args args) {
+  using Cf = Cfg<kMx, kBN>;
+  constexpr int S = Cf::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* ring_a = smem;
+  uint8_t* ring_b = ring_a + S * Cf::kStageA;
+  uint8_t* ring_sfa = ring_b + S * Cf::kStageB;
+  uint8_t* ring_sfb = ring_sfa + S * Cf::kStageSfa;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring_sfb + S * Cf::kStageSfb);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  volatile uint32_t* unit_status = tmem_slot + 2;   // two slots, indexed by accumulator
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t cta = blockIdx.x;
+  const Plan& plan = args.plan;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kEpilogueThreads / 32);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    unit_status[0] = 0;
+    unit_status[1] = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cf::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      Cursor cur(plan, cta);
+      Unit u;
+      while (ok && cur.next(plan, u)) {
+        int32_t tm, tn;
+        tile_coords(plan, u.tile, tm, tn);
+        for (int32_t k = u.k0; k < u.k1; ++k) {
+          if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, args, kSiteProducer)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], Cf::kStageBytes);
+          uint8_t* sa = ring_a + stage * Cf::kStageA;
+          uint8_t* sb = ring_b + stage * Cf::kStageB;
+          if constexpr (kMx) {
+            tma_load_2d(sa, &tmA, &full[stage], k * 128, tm * kBM);
+            tma_load_2d(sb, &tmB, &full[stage], k * 128, tn * kBN);
+            bulk_load(ring_sfa + stage * Cf::kStageSfa,
+                      args.sfa + (static_cast<int64_t>(tm) * args.sf_kgroups + 2 * k) * 512, 1024,
+                      &full[stage]);
+#pragma unroll
+            for (int j = 0; j < kBN / 128; ++j) {
+              const int64_t nb = static_cast<int64_t>(tn) * (kBN / 128) + j;
+              bulk_load(ring_sfb + stage * Cf::kStageSfb + j * 1024,
+                        args.sfb + (nb * args.sf_kgroups + 2 * k) * 512, 1024, &full[stage]);
+            }
+          } else {
+            tma_load_2d(sa, &tmA, &full[stage], k * 64, tm * kBM);
+#pragma unroll
+            for (int j = 0; j < kBN / 64; ++j)
+              tma_load_2d(sb + j * 8192, &tmB, &full[stage], tn * kBN + j * 64, k * 64);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Let the copies already issued land before the CTA's shared memory goes away.
+        const int64_t outstanding = issued < S ? issued : S;
+        for (int64_t i = 1; i <= outstanding; ++i) {
+          const int s = static_cast<int>((stage - i + S) % S);
+          const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+          if (!wait_bar_drain(&full[s], par, 100000000ull)) record_error(args, kSiteDrain, -1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      Cursor cur(plan, cta);
+      Unit u;
+      while (ok && cur.next(plan, u)) {
+        if (!wait_bar(&tempty[acc], acc_phase ^ 1u, abort_flag, args, kSiteMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * Cf::kAccCols;
+        for (int32_t k = u.k0; k < u.k1; ++k) {
+          if (!wait_bar(&full[stage], phase, abort_flag, args, kSiteMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(ring_a + stage * Cf::kStageA);
+          const uint32_t b0 = smem_addr(ring_b + stage * Cf::kStageB);
+          if constexpr (kMx) {
+            // Scale blocks of this stage -> tensor memory slot `stage` (each 512-byte group
+            // holds 128 rows x 4 scale bytes, rows r, r+32, r+64, r+96 in one 16-byte line).
+            const uint32_t sfa_t = tmem_base + 2 * Cf::kAccCols + stage * Cf::kSfaCols;
+            const uint32_t sfb_t = tmem_base + 2 * Cf::kAccCols + S * Cf::kSfaCols + stage * Cf::kSfbCols;
+            const uint32_t sfa_s = smem_addr(ring_sfa + stage * Cf::kStageSfa);
+            const uint32_t sfb_s = smem_addr(ring_sfb + stage * Cf::kStageSfb);
+#pragma unroll
+            for (int g = 0; g < 2; ++g)
+              tmem_copy_32x128b_x4(sfa_t + g * 4, smem_desc(sfa_s + g * 512, 0, 128, kLayoutSwizzleNone));
+#pragma unroll
+            for (int j = 0; j < kBN / 128; ++j)
+#pragma unroll
+              for (int g = 0; g < 2; ++g)
+                tmem_copy_32x128b_x4(sfb_t + g * (kBN / 32) + j * 4,
+                                     smem_desc(sfb_s + j * 1024 + g * 512, 0, 128, kLayoutSwizzleNone));
+#pragma unroll
+            for (int j = 0; j < Cf::kMmasPerStage; ++j) {
+              const uint32_t g = j >> 1;
+              const uint32_t sf_id = (j & 1) * 2;
+              const uint32_t idesc = Cf::kIdesc | (sf_id << 29) | (sf_id << 4);
+              const uint64_t ad = smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
+              const uint64_t bd = smem_desc(b0 + j * 32, 16, 1024, kLayoutSwizzle128B);
+              mma_mxf4(d_tmem, ad, bd, idesc, sfa_t + g * 4, sfb_t + g * (kBN / 32),
+                       (k > u.k0 || j > 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < Cf::kMmasPerStage; ++j) {
+              // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; K advances 32 B.
+              // B: MN-major, 128-byte swizzle; 64-column blocks 8 KB apart (leading offset),
+              //    8-row K groups 1024 B apart (stride offset); K advances 16 rows = 2 KB.
+              const uint64_t ad = smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
+              const uint64_t bd = smem_desc(b0 + j * 2048, 8192, 1024, kLayoutSwizzle128B);
+              mma_f16(d_tmem, ad, bd, Cf::kIdesc, (k > u.k0 || j > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // Every MMA this thread issued has completed once mma_done flips.
+      mma_commit(mma_done);
+      if (!wait_bar_drain(mma_done, 0, 100000000ull)) record_error(args, kSiteDrain, -1);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    // Thread 0 of the epilogue does the waits of a piece (accumulator ready; for an owner,
+    // the contributors' flags) and publishes the outcome in unit_status[acc]; a named barrier
+    // then makes the decision uniform, so no epilogue thread can be left at a barrier.
+    const int quarter = warp & 3;               // TMEM lanes this warp may read
+    const int row = quarter * 32 + lane;        // tile row of this thread
+    const int et = threadIdx.x - 64;            // 0..127
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    Cursor cur(plan, cta);
+    Unit u;
+    while (cur.next(plan, u)) {
+      // Contributions to an owned tile come from CTAs cta+1, cta+2, ... until k is covered.
+      int n_contrib = 0;
+      if (u.role == kRoleOwner) {
+        int64_t covered = u.k1;
+        for (int64_t c = cta + 1; covered < plan.iters; ++c, ++n_contrib) {
+          const int64_t len = sk_range_len(plan, c);
+          covered += (len < plan.iters - covered) ? len : (plan.iters - covered);
+        }
+      }
+      if (et == 0) {
+        uint32_t status = kUnitStore;
+        if (!wait_bar(&tfull[acc], acc_phase, abort_flag, args, kSiteEpilogue)) {
+          status = kUnitAbort;
+        } else if (u.role == kRoleOwner) {
+          for (int c = 0; c < n_contrib; ++c) {
+            uint32_t* f = args.flags + cta + 1 + c;
+            if (!wait_flag(f, args.epoch, args.timeout_ns)) {
+              record_error(args, kSiteFlag, u.tile);
+              status = kUnitSkip;
+              break;
+            }
+            *reinterpret_cast<volatile uint32_t*>(f) = 0u;  // consumed: ready for the next launch
+          }
+        }
+        unit_status[acc] = status;
+      }
+      named_barrier_sync(1, kEpilogueThreads);
+      const uint32_t status = unit_status[acc];
+      if (status == kUnitAbort) break;
+      tc_fence_after();
+      int32_t tm, tn;
+      tile_coords(plan, u.tile, tm, tn);
+      const int64_t m = static_cast<int64_t>(tm) * kBM + row;
+      const int64_t n_tile = static_cast<int64_t>(tn) * kBN;
+      const bool do_store = (status == kUnitStore);
+
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc) * Cf::kAccCols;
+      float4* my_slot = reinterpret_cast<float4*>(args.P + cta * (kBM * kBN));
+#pragma unroll 1
+      for (int ch = 0; ch < kBN / 32; ++ch) {
+        uint32_t r[32];
+        tmem_load_32cols(t_row + ch * 32, r);
+        tmem_load_wait();
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        if (u.role == kRoleContrib) {
+          // Slot layout [chunk][column quad][row]: one warp store covers 512 contiguous bytes.
+          float4* dst = my_slot + static_cast<int64_t>(ch) * 8 * kBM + row;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            __stcg(dst + q * kBM, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+        } else if (do_store) {
+          for (int c = 0; c < n_contrib; ++c) {
+            const float4* src = reinterpret_cast<const float4*>(args.P + (cta + 1 + c) * (kBM * kBN)) +
+                                static_cast<int64_t>(ch) * 8 * kBM + row;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 p = __ldcg(src + q * kBM);
+              v[4 * q] += p.x;
+              v[4 * q + 1] += p.y;
+              v[4 * q + 2] += p.z;
+              v[4 * q + 3] += p.w;
+            }
+          }
+          store_row_chunk(args, m, n_tile + ch * 32, v);
+        }
+      }
+      // Accumulator drained: hand it back to the MMA warp.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (u.role == kRoleContrib) {
+        // Publish the partial: every thread's stores, then one release at GPU scope.
+        __threadfence();
+        named_barrier_sync(1, kEpilogueThreads);
+        if (et == 0 && !(args.inject_drop && cta == args.drop_cta))
+          flag_release(args.flags + cta, args.epoch);
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cf::kTmemCols);
+  }
+}
+
+}  // namespace sk

@@ -1,0 +1,104 @@
+// Tile scheduler shared by the host planner and the kernels (__host__ __device__).
+//
+// A plan fixes, for a problem of tiles_m x tiles_n output tiles with `iters` k-iterations
+// each and a grid of g CTAs, which (tile, k-range) pieces every CTA runs and in which order:
+//   * linear tiles [0, whole_tiles) run whole, CTA c taking c, c+g, c+2g, ... (this covers the
+//     data-parallel schedule, where g = tiles, and the SM-constrained persistent schedule of
+//     flashinfer PR #982 "SM-constraint-GEMM by triton persistent kernel");
+//   * linear tiles [whole_tiles, tiles) form the Stream-K region: its tiles x iters
+//     iterations, in tile-major order, are cut into g contiguous ranges, CTA c's range holding
+//     sk_base iterations plus one if c < sk_extra.  Each CTA runs its Stream-K range first.
+// A piece holding k = 0 makes its CTA the tile's owner; a piece starting past k = 0 is a
+// partial that the owner adds in before the bias (tritonBLAS PR #67 "Fix StreamK Kernel
+// Bias", Technical Details).  Because ranges are contiguous, only a CTA's first piece can
+// start inside a tile, so a CTA spills at most once (one scratch slot per CTA, as in
+// tritonBLAS PR #74 "Stream-k mxfp4 kernel"), and an owner's split tile is its last Stream-K
+// piece, continued by CTAs c+1, c+2, ...
+//
+// Linear tile index -> (tile row, tile column) uses a grouped raster: groups of `group_m`
+// tile rows, column-major inside a group, so CTAs running at the same time share operand
+// panels in L2.  The raster changes only the fp32 summation grouping of nothing: every tile
+// is still summed over k in ascending order.
+#pragma once
+
+#include <cstdint>
+
+namespace sk {
+
+enum : int32_t { kRoleFull = 0, kRoleOwner = 1, kRoleContrib = 2 };
+
+struct Plan {
+  int32_t tiles_m, tiles_n;
+  int32_t iters;        // k-iterations per tile
+  int32_t grid;         // CTAs launched
+  int32_t group_m;      // raster group height in tiles
+  int32_t pad_;
+  int64_t tiles;        // tiles_m * tiles_n
+  int64_t whole_tiles;  // linear tiles [0, whole_tiles) run whole
+  int64_t sk_base;      // Stream-K iterations per CTA
+  int64_t sk_extra;     // CTAs [0, sk_extra) take one more
+};
+
+struct Unit {
+  int64_t tile;   // linear tile index
+  int32_t k0, k1; // k-iteration range [k0, k1)
+  int32_t role;
+};
+
+__host__ __device__ __forceinline__ int64_t sk_range_begin(const Plan& p, int64_t cta) {
+  return cta * p.sk_base + (cta < p.sk_extra ? cta : p.sk_extra);
+}
+
+__host__ __device__ __forceinline__ int64_t sk_range_len(const Plan& p, int64_t cta) {
+  return p.sk_base + (cta < p.sk_extra ? 1 : 0);
+}
+
+// Walks one CTA's pieces in execution order.
+struct Cursor {
+  int64_t it, end;   // remaining Stream-K iterations [it, end), relative to the region
+  int64_t next_whole;
+
+  __host__ __device__ __forceinline__ Cursor(const Plan& p, int64_t cta) {
+    it = sk_range_begin(p, cta);
+    end = it + sk_range_len(p, cta);
+    next_whole = cta;
+  }
+
+  __host__ __device__ __forceinline__ bool next(const Plan& p, Unit& u) {
+    if (it < end) {
+      const int64_t t = it / p.iters;
+      const int32_t k0 = static_cast<int32_t>(it - t * p.iters);
+      const int64_t left = end - it;
+      const int32_t k1 = (left >= p.iters - k0) ? p.iters : k0 + static_cast<int32_t>(left);
+      u.tile = p.whole_tiles + t;
+      u.k0 = k0;
+      u.k1 = k1;
+      u.role = (k0 > 0) ? kRoleContrib : (k1 == p.iters ? kRoleFull : kRoleOwner);
+      it += k1 - k0;
+      return true;
+    }
+    if (next_whole < p.whole_tiles) {
+      u.tile = next_whole;
+      u.k0 = 0;
+      u.k1 = p.iters;
+      u.role = kRoleFull;
+      next_whole += p.grid;
+      return true;
+    }
+    return false;
+  }
+};
+
+__host__ __device__ __forceinline__ void tile_coords(const Plan& p, int64_t t, int32_t& tm,
+                                                     int32_t& tn) {
+  const int64_t per_group = static_cast<int64_t>(p.group_m) * p.tiles_n;
+  const int64_t group = t / per_group;
+  const int64_t first_m = group * p.group_m;
+  const int64_t rows_here =
+      (p.tiles_m - first_m < p.group_m) ? (p.tiles_m - first_m) : p.group_m;
+  const int64_t r = t - group * per_group;
+  tm = static_cast<int32_t>(first_m + r % rows_here);
+  tn = static_cast<int32_t>(r / rows_here);
+}
+
+}  // namespace sk

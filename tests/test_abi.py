@@ -1,0 +1,151 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every function the header
+declares, rejects bad arguments before touching CUDA, and its scheduler (the code the kernels
+run) produces the same work split as the oracle's independent restatement."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import sm_constrained_persistent_gb300 as sk
+from sm_constrained_persistent_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return sk.lib()
+
+
+def _declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(sk_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ["sk_gemm_bf16", "sk_gemm_mxfp4", "sk_stream_status", "sk_workspace_reserve",
+                     "sk_workspace_release_all", "sk_status_string", "sk_plan", "sk_plan_segments",
+                     "sk_gemm_bf16_ex", "sk_gemm_mxfp4_ex"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert sk.sk_status_string(code)
+    assert sk.sk_status_string(99) == "unknown status"
+
+
+P = 0x100000  # a 16-byte aligned fake device address: never dereferenced by these tests
+
+
+@pytest.mark.parametrize("args", [
+    dict(A=None), dict(B=None), dict(C=None),
+    dict(A=P + 8), dict(B=P + 2), dict(C=P + 4), dict(bias=P + 1),
+    dict(M=0), dict(N=0), dict(K=0), dict(M=-5), dict(K=2 ** 31),
+    dict(K=100), dict(N=100),            # bf16 needs 16-byte row pitches
+    dict(out_dtype=2), dict(mode=4), dict(mode=-1),
+])
+def test_bf16_bad_arguments_are_rejected_before_cuda(lib, args):
+    a = dict(A=P, B=P, bias=None, C=P, out_dtype=1, M=64, N=64, K=64, num_sms=0, mode=2)
+    a.update(args)
+    st = sk.sk_gemm_bf16(a["A"], a["B"], a["bias"], a["C"], a["out_dtype"], a["M"], a["N"],
+                         a["K"], a["num_sms"], a["mode"], None)
+    assert st == sk.SK_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args", [
+    dict(A_scale=None), dict(B_scale=None), dict(K=48), dict(K=16), dict(tile_n=256),
+    dict(tile_n=64),
+])
+def test_mxfp4_bad_arguments_are_rejected_before_cuda(lib, args):
+    a = dict(A=P, A_scale=P, B=P, B_scale=P, C=P, M=10, N=30, K=64, tile_n=0)
+    a.update(args)
+    opts = {"tile_n": a["tile_n"]}
+    st = sk.sk_gemm_mxfp4_ex(a["A"], a["A_scale"], a["B"], a["B_scale"], None, a["C"], 1,
+                             a["M"], a["N"], a["K"], 0, 2, opts, None)
+    assert st == sk.SK_ERR_INVALID_ARG
+
+
+def test_valid_call_without_a_gpu_is_unsupported_not_a_crash(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = sk.sk_gemm_bf16(P, P, None, P, 1, 64, 64, 64, 0, 2, None)
+    assert st == sk.SK_ERR_UNSUPPORTED
+
+
+def test_options_validation(lib):
+    st = sk.sk_gemm_bf16_ex(P, P, None, P, 1, 64, 64, 64, 0, 2,
+                            {"spin_timeout_ns": -1}, None)
+    assert st == sk.SK_ERR_INVALID_ARG
+    assert sk.sk_workspace_reserve(0, None, 0) == sk.SK_ERR_INVALID_ARG
+
+
+# ---- planning -----------------------------------------------------------------------------
+
+def test_plan_fields_follow_the_schedule_rules(lib):
+    # grid capped at the SM count (a request of 133 on a 132-SM part launches 132)
+    p = sk.sk_plan(0, 4096, 4096, 4096, 133, "persistent", 132, {"tile_n": 128})
+    assert p.grid == 132 and p.tiles == 1024 and p.iters == 64
+    p = sk.sk_plan(0, 4096, 4096, 4096, 0, "dp", 148, {"tile_n": 128})
+    assert p.grid == 1024
+    p = sk.sk_plan(0, 256, 256, 512, 3, "streamk", 148)
+    assert (p.tile_n, p.tiles, p.iters, p.grid) == (128, 4, 8, 3)
+    assert (p.sk_base, p.sk_extra, p.whole_tiles) == (10, 2, 0)
+    p = sk.sk_plan(0, 1920, 1920, 16384, 0, "hybrid", 148)
+    assert p.tiles == 225 and p.sk_tiles == 225 % 148 and p.whole_tiles == 148
+    p = sk.sk_plan(1, 8192, 8192, 8192, 0, "streamk", 148)
+    assert (p.tile_n, p.tile_k, p.iters) == (128, 256, 32)
+    with pytest.raises(sk.SkError):
+        sk.sk_plan(0, 0, 8, 8, 0, "dp", 148)
+
+
+def _same_split(mode, M, N, K, g_req, sms, tile_n):
+    plan = sk.sk_plan(0, M, N, K, g_req, mode, sms, {"tile_n": tile_n})
+    got = sk.sk_plan_segments(plan)
+    want = oracle.schedule(sk.MODES[mode], plan.tiles, plan.iters, plan.grid)
+    assert np.array_equal(got[:, :5], want), (mode, M, N, K, g_req, sms)
+    return plan, got
+
+
+@pytest.mark.parametrize("mode", ["dp", "persistent", "streamk", "hybrid"])
+@pytest.mark.parametrize("shape", [(256, 256, 512), (1920, 1920, 16384), (64, 14336, 4096),
+                                   (200, 136, 200), (128, 128, 64), (4096, 4096, 4096)])
+@pytest.mark.parametrize("g", [1, 3, 7, 16, 132, 0])
+def test_kernel_scheduler_matches_oracle_restatement(lib, mode, shape, g):
+    M, N, K = shape
+    _same_split(mode, M, N, K, g, 148, 128)
+
+
+def test_raster_is_a_bijection_onto_the_tile_grid(lib):
+    for (M, N, group) in [(8192, 8192, 16), (1920, 1920, 16), (1000, 3000, 5), (128, 256, 1),
+                          (640, 128, 3)]:
+        plan = sk.sk_plan(0, M, N, 64, 0, "dp", 148, {"tile_n": 128, "raster_group": group})
+        segs = sk.sk_plan_segments(plan)
+        cells = set(map(tuple, segs[:, 5:7].tolist()))
+        assert len(cells) == plan.tiles
+        assert cells == {(i, j) for i in range(plan.tiles_m) for j in range(plan.tiles_n)}
+
+
+def test_streamk_256_cube_split_matches_golden(lib):
+    want = np.loadtxt(os.path.join(ROOT, "tests", "golden", "streamk_256x256x512_g3.txt"),
+                      dtype=np.int64)
+    plan = sk.sk_plan(0, 256, 256, 512, 3, "streamk", 148)
+    got = sk.sk_plan_segments(plan)
+    assert np.array_equal(got[:, :5], want)
