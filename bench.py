@@ -1,0 +1,508 @@
+"""Benchmark of the GB300 addmm GEMM path (bf16 / MXFP4, persistent / Stream-K schedules).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--mode streamk] [--no-extras]
+
+One step is one addmm of the workload (default: bf16 8192 x 8192 x 8192 with a bf16 bias,
+bf16 output, Stream-K over all SMs).  Inputs are resident in HBM when the timed region starts;
+A + B + C (384 MiB) exceed the 129 MB L2, so no flush is needed between steps.  Prints one JSON
+line (rank 0).  Under torchrun every rank runs an independent replica on its own GPU (the GEMM
+has no exchange step); the value is the sum of the ranks' work over the slowest rank's time.
+
+--impl reference times the CPU oracle (plain binary64 C++ on the host cores) on a bounded
+sample of the same workload: the comparison arm, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE_METRIC = "GEMM TFLOPS (bf16, MXFP4) per schedule and % of GB300 dense tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# fp4 dense peak relative to bf16 dense (nominal 13.5 / 2.25 PFLOP/s; MXFP4 with E8M0 scales
+# runs at the fp4 rate)
+FP4_OVER_BF16 = 13.5 / 2.25
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="addmm_bf16_8192")
+    ap.add_argument("--mode", default="streamk", choices=["dp", "persistent", "streamk", "hybrid"])
+    ap.add_argument("--num-sms", type=int, default=0)
+    ap.add_argument("--no-extras", action="store_true", help="skip the per-schedule extras")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value, device=None):
+    """Largest value over all ranks (the job's time is set by its slowest replica)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, value, device=None):
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sm_constrained_persistent_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    entry = d.get("kernels", {}).get(kernel_key)
+    return None if entry is None else entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, smax = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            mx = smax
+            sms.append(sm)
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        load = [s for s in sms if s >= 0.5 * max(sms)]
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def tile_efficiency(plan, sm_count):
+    """Tile-quantisation efficiency: useful k-iterations / (SMs used x busiest SM's iterations)."""
+    import sm_constrained_persistent_gb300 as sk
+    segs = sk.sk_plan_segments(plan)
+    per_cta = np.zeros(plan.grid, dtype=np.int64)
+    np.add.at(per_cta, segs[:, 0], segs[:, 3] - segs[:, 2])
+    total = int(per_cta.sum())
+    if plan.grid > sm_count:   # data-parallel: CTAs run in waves of one per SM
+        per_sm = np.zeros(sm_count, dtype=np.int64)
+        np.add.at(per_sm, np.arange(plan.grid) % sm_count, per_cta)
+        return total / (sm_count * int(per_sm.max()))
+    return total / (plan.grid * int(per_cta.max()))
+
+
+# ---------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------
+
+class Problem:
+    """Device-resident inputs and output of one workload, plus pinned host copies (for e2e)."""
+
+    def __init__(self, name, device):
+        import torch
+        from sm_constrained_persistent_gb300 import inputs
+        p = inputs.workload(name)
+        self.name, self.p, self.device = name, p, device
+        self.fmt, self.M, self.N, self.K = p["format"], p["M"], p["N"], p["K"]
+        self.out_dtype = torch.bfloat16 if p["out_dtype"] == "bf16" else torch.float32
+
+        def pinned(x, dtype=None):
+            t = torch.from_numpy(np.ascontiguousarray(x))
+            if dtype is not None:
+                t = t.view(dtype)
+            return t.pin_memory()
+
+        if self.fmt == "bf16":
+            self.host = {"A": pinned(p["A"].view(np.int16), torch.bfloat16),
+                         "B": pinned(p["B"].view(np.int16), torch.bfloat16)}
+        else:
+            self.host = {"A": pinned(p["A"]), "A_scale": pinned(p["A_scale"]),
+                         "B": pinned(p["B"]), "B_scale": pinned(p["B_scale"])}
+        b = p["bias"]
+        if b is not None:
+            self.host["bias"] = pinned(b.view(np.int16), torch.bfloat16) if b.dtype == np.uint16 \
+                else pinned(b)
+        self.dev = {k: v.to(device) for k, v in self.host.items()}
+        self.C = torch.empty((self.M, self.N), dtype=self.out_dtype, device=device)
+        self.C_host = torch.empty((self.M, self.N), dtype=self.out_dtype).pin_memory()
+        self.flops = 2.0 * self.M * self.N * self.K
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host.values())
+
+    def d2h_bytes(self):
+        return self.C.numel() * self.C.element_size()
+
+    def call(self, mode, num_sms, stream_ptr, dev=None):
+        """One addmm through the C ABI.  Returns the status code."""
+        import sm_constrained_persistent_gb300 as sk
+        d = self.dev if dev is None else dev
+        bias = d["bias"].data_ptr() if "bias" in d else None
+        od = sk.SK_BF16 if self.out_dtype.itemsize == 2 else sk.SK_F32
+        m = sk.MODES[mode]
+        if self.fmt == "bf16":
+            return sk.sk_gemm_bf16(d["A"].data_ptr(), d["B"].data_ptr(), bias, self.C.data_ptr(),
+                                   od, self.M, self.N, self.K, num_sms, m, stream_ptr)
+        return sk.sk_gemm_mxfp4(d["A"].data_ptr(), d["A_scale"].data_ptr(), d["B"].data_ptr(),
+                                d["B_scale"].data_ptr(), bias, self.C.data_ptr(), od, self.M,
+                                self.N, self.K, num_sms, m, stream_ptr)
+
+    def kernels_per_call(self):
+        return 1 if self.fmt == "bf16" else 3   # MXFP4: two scale-layout kernels + the GEMM
+
+
+def time_calls(prob, mode, num_sms, steps, warmup, dist=None):
+    """Device time of `steps` back-to-back calls (after `warmup`), CUDA events on the launch
+    stream, barrier + synchronize on both sides.  Returns (total ms, per-call ms list)."""
+    import torch
+    import sm_constrained_persistent_gb300 as sk
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    for _ in range(warmup):
+        st = prob.call(mode, num_sms, sp)
+        if st != 0:
+            raise RuntimeError(f"warm-up call failed: {sk.STATUS.get(st, st)}")
+    torch.cuda.synchronize()
+    if sk.sk_stream_status(sp) != 0:
+        raise RuntimeError("kernel reported an error during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    for s, e in ev:
+        s.record(stream)
+        prob.call(mode, num_sms, sp)
+        e.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    if sk.sk_stream_status(sp) != 0:
+        raise RuntimeError("kernel reported an error in the timed region")
+    per = [s.elapsed_time(e) for s, e in ev]
+    total = ev[0][0].elapsed_time(ev[-1][1])
+    return total, per
+
+
+def time_e2e(prob, mode, num_sms, steps, warmup):
+    """Same metric end to end: pinned host inputs -> device, addmm, C -> pinned host, all on
+    the launch stream inside the timed region."""
+    import torch
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    staging = {k: torch.empty_like(v) for k, v in prob.dev.items()}
+
+    def one():
+        for k, v in prob.host.items():
+            staging[k].copy_(v, non_blocking=True)
+        prob.call(mode, num_sms, sp, dev=staging)
+        prob.C_host.copy_(prob.C, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / steps
+
+
+def cpu_baseline(prob, seconds):
+    """The oracle, as it stands, on a block of rows of the same workload (about `seconds` of
+    host time).  Returns the cpu_baseline object in the metric's unit."""
+    import oracle
+    p = prob.p
+    threads = oracle.hardware_threads()
+
+    def run(rows):
+        t0 = time.perf_counter()
+        if prob.fmt == "bf16":
+            oracle.addmm_bf16(p["A"], p["B"], p["bias"], rows=(0, rows), threads=threads)
+        else:
+            oracle.addmm_mxfp4(p["A"], p["A_scale"], p["B"], p["B_scale"], p["bias"],
+                               rows=(0, rows), threads=threads)
+        return time.perf_counter() - t0
+
+    probe_rows = min(prob.M, max(threads, 8))
+    t_probe = run(probe_rows)
+    rows = int(min(prob.M, max(probe_rows, probe_rows * seconds / max(t_probe, 1e-3))))
+    rows = max(threads, rows - rows % threads) if rows >= threads else rows
+    t = run(rows)
+    flops = 2.0 * rows * prob.N * prob.K
+    return {"value": flops / t / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+            "sample": f"rows [0, {rows}) of the {prob.M}x{prob.N}x{prob.K} {prob.fmt} addmm "
+                      f"({flops / 1e9:.1f} GFLOP, {t:.1f} s, binary64 accumulation)"}
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    import __graft_entry__
+    __graft_entry__.build()          # no-op when the library is up to date
+    import sm_constrained_persistent_gb300 as sk
+
+    props = torch.cuda.get_device_properties(local)
+    sm_count = props.multi_processor_count
+    prob = Problem(args.workload, device)
+    torch.cuda.synchronize()
+
+    with ClockSampler(local) as clocks:
+        total_ms, per = time_calls(prob, args.mode, args.num_sms, args.steps, args.warmup, dist)
+    ms_max = max_over_ranks(dist, total_ms / args.steps, device)
+    flops_all = sum_over_ranks(dist, prob.flops * args.steps, device)
+    value = flops_all / (ms_max * args.steps * 1e-3) / 1e12
+    clock = clocks.summary()
+
+    plan = sk.sk_plan(0 if prob.fmt == "bf16" else 1, prob.M, prob.N, prob.K, args.num_sms,
+                      args.mode, sm_count)
+    peaks, peak_src = measured_peaks()
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    if prob.fmt == "bf16":
+        peak, peak_note = bf16_peak, f"bf16 dense, burst, {peak_src}"
+    else:
+        peak = bf16_peak * FP4_OVER_BF16
+        peak_note = f"fp4 dense = {peak_src} bf16 burst x {FP4_OVER_BF16:g} (nominal ratio)"
+    gemm_ms = statistics.mean(per)   # one GEMM kernel dominates each call
+    achieved = prob.flops / (gemm_ms * 1e-3) / 1e12
+    kernel_key = f"gemm_kernel<{'mxf4' if prob.fmt != 'bf16' else 'bf16'},{plan.tile_n}>:{args.workload}:{args.mode}"
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": recorded_traffic(kernel_key), "peak_source": peak_note,
+                "kernel": kernel_key}
+
+    e2e_ms = time_e2e(prob, args.mode, args.num_sms, max(3, min(args.steps, 10)), 2)
+    e2e_ms_max = max_over_ranks(dist, e2e_ms, device)
+    e2e = {"value": round(sum_over_ranks(dist, prob.flops, device) / (e2e_ms_max * 1e-3) / 1e12, 2),
+           "unit": "TFLOPS", "h2d_bytes_per_step": prob.h2d_bytes(),
+           "d2h_bytes_per_step": prob.d2h_bytes()}
+
+    result = {
+        "metric": HEADLINE_METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if prob.fmt == "bf16" else "mxfp4(e2m1+e8m0)", "data": "synthetic",
+        "config": {"workload": args.workload, "M": prob.M, "N": prob.N, "K": prob.K,
+                   "format": prob.fmt, "out": str(prob.out_dtype).replace("torch.", ""),
+                   "bias": prob.p["bias"] is not None, "mode": args.mode,
+                   "num_sms": args.num_sms if args.num_sms > 0 else sm_count,
+                   "grid": plan.grid, "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}",
+                   "tile_quant_eff": round(tile_efficiency(plan, sm_count), 4),
+                   "pct_of_dense_peak": round(100 * value / world / peak, 2),
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas{world}"},
+        "roofline": roofline, "e2e": e2e,
+        "gpu_launches": args.steps * prob.kernels_per_call(),
+        "clocks": {"sm_mhz": clock["sm_mhz"], "sm_max_mhz": clock["sm_max_mhz"],
+                   "reasons": clock["reasons"]},
+    }
+    if not args.no_extras:
+        result["extras"] = extras(prob, sm_count, dist)
+    if world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(prob, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def extras(prob, sm_count, dist):
+    """Per-schedule throughput of the benchmark workloads (each timed on its own after the
+    headline region: 3 warm-up + 10 timed calls)."""
+    import torch
+    import sm_constrained_persistent_gb300 as sk
+    out = {}
+    peaks, _ = measured_peaks()
+    bpeak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    jobs = [(prob.name, prob, ["dp", "persistent", "streamk", "hybrid"])]
+    for name, modes in [("gemm_bf16_1920x1920x16384", ["dp", "persistent", "streamk", "hybrid"]),
+                        ("addmm_mxfp4_8192", ["dp", "persistent", "streamk", "hybrid"])]:
+        if name != prob.name:
+            jobs.append((name, None, modes))
+    for name, pr, modes in jobs:
+        if pr is None:
+            pr = Problem(name, prob.device)
+        peak = bpeak if pr.fmt == "bf16" else bpeak * FP4_OVER_BF16
+        res = {}
+        for mode in modes:
+            total, per = time_calls(pr, mode, 0, 10, 3, dist)
+            ms = total / 10
+            plan = sk.sk_plan(0 if pr.fmt == "bf16" else 1, pr.M, pr.N, pr.K, 0, mode, sm_count)
+            tflops = pr.flops / (ms * 1e-3) / 1e12
+            res[mode] = {"ms": round(ms, 4), "tflops": round(tflops, 1),
+                         "pct_peak": round(100 * tflops / peak, 1), "grid": plan.grid,
+                         "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}",
+                         "tile_quant_eff": round(tile_efficiency(plan, sm_count), 4)}
+        out[name] = res
+        if pr is not prob:
+            del pr
+            torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return
+    import oracle
+    from sm_constrained_persistent_gb300 import inputs
+    p = inputs.workload(args.workload)
+    threads = oracle.hardware_threads()
+    rows = max(threads, 16)
+    M, N, K = p["M"], p["N"], p["K"]
+
+    def step():
+        if p["format"] == "bf16":
+            oracle.addmm_bf16(p["A"], p["B"], p["bias"], rows=(0, rows), threads=threads)
+        else:
+            oracle.addmm_mxfp4(p["A"], p["A_scale"], p["B"], p["B_scale"], p["bias"],
+                               rows=(0, rows), threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = 2.0 * rows * N * K
+    value = flops / dt / 1e12
+    sample = (f"rows [0, {rows}) of the {M}x{N}x{K} {p['format']} addmm per step "
+              f"({flops / 1e9:.2f} GFLOP), binary64 accumulation")
+    print(json.dumps({
+        "impl": "reference", "metric": HEADLINE_METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "N": N, "K": K, "format": p["format"],
+                   "mode": args.mode},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

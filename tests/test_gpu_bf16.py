@@ -1,0 +1,216 @@
+"""GPU parity of the bf16 addmm path against the CPU oracle, through the C ABI.
+
+Covers every schedule (data-parallel, SM-constrained persistent, Stream-K, hybrid), both CTA
+tile widths, fp32 and bf16 outputs, ragged shapes, a num_sms sweep, repeated launches, two
+streams, CUDA-graph replay, a Stream-K wait that is made to run out, and the full-size
+workloads on sampled outputs."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as gu
+import oracle
+import sm_constrained_persistent_gb300 as sk
+from sm_constrained_persistent_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+MODES = ["dp", "persistent", "streamk", "hybrid"]
+
+
+@pytest.fixture(autouse=True)
+def _device(cuda_device):
+    yield
+
+
+# ---- the 256 x 256 x 512 fp32-output addmm: Stream-K over 3 CTAs, tiles split in K ----------
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("num_sms", [3, 0])
+def test_addmm_256_fp32_out_matches_oracle(mode, num_sms):
+    p = inputs.workload("addmm_bf16_256x256x512_f32out")
+    c = gu.run_bf16(p, out="f32", mode=mode, num_sms=num_sms)
+    ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "f32")
+    gu.assert_close(gu.host_values(c), ref, "f32", f"{mode}/{num_sms}")
+
+
+def test_addmm_256_streamk_over_3_ctas_splits_two_tiles():
+    plan = sk.sk_plan(0, 256, 256, 512, 3, "streamk", torch.cuda.get_device_properties(0).multi_processor_count)
+    segs = sk.sk_plan_segments(plan)
+    assert plan.grid == 3 and plan.tile_n == 128
+    assert (segs[:, 4] == 1).sum() == 2 and (segs[:, 4] == 2).sum() == 2
+
+
+# ---- exact integer inputs: bit-exact in every schedule --------------------------------------
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", [(200, 136, 200), (1, 8, 8), (128, 128, 64), (129, 264, 72),
+                                   (384, 1024, 512), (640, 256, 8)])
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_integer_inputs_are_bit_exact(mode, shape, tile_n, out):
+    M, N, K = shape
+    p = inputs.bf16_problem(M, N, K, seed=M + 7 * N + 13 * K, integer=True,
+                            bias="bf16_int" if out == "bf16" else "f32_int")
+    c = gu.run_bf16(p, out=out, mode=mode, num_sms=5, options={"tile_n": tile_n})
+    want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]),
+                               oracle.BF16 if out == "bf16" else oracle.F32)
+    want_bits = want if out == "bf16" else want.view(np.uint32)
+    assert np.array_equal(gu.host_bits(c), want_bits)
+
+
+@pytest.mark.parametrize("mode", ["persistent", "streamk", "hybrid"])
+@pytest.mark.parametrize("num_sms", [1, 2, 3, 7, 16, 64, 151, 152, 0, 1000])
+def test_num_sms_sweep_integer_bit_exact(mode, num_sms):
+    p = inputs.bf16_problem(520, 776, 1000, seed=77, integer=True, bias="bf16_int")
+    c = gu.run_bf16(p, out="bf16", mode=mode, num_sms=num_sms)
+    want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), oracle.BF16)
+    assert np.array_equal(gu.host_bits(c), want)
+
+
+def test_no_bias_and_zero_a_give_bias_rows():
+    M, N, K = 300, 264, 136
+    p = inputs.bf16_problem(M, N, K, seed=3, bias="bf16_uniform")
+    p["A"] = np.zeros_like(p["A"])
+    for mode in MODES:
+        c = gu.run_bf16(p, out="bf16", mode=mode, num_sms=7)
+        assert np.array_equal(gu.host_bits(c), np.broadcast_to(p["bias"], (M, N)))
+    p["bias"] = None
+    c = gu.run_bf16(p, out="f32", mode="streamk", num_sms=7)
+    assert not gu.host_values(c).any()
+
+
+# ---- random inputs --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_random_inputs_match_oracle(mode, tile_n):
+    p = inputs.bf16_problem(640, 896, 1544, seed=5, operand_scale="sqrt_k", bias="bf16_uniform")
+    c = gu.run_bf16(p, out="bf16", mode=mode, num_sms=0, options={"tile_n": tile_n})
+    ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "bf16")
+    gu.assert_close(gu.host_values(c), ref, "bf16", mode)
+
+
+def test_streamk_and_dp_outputs_agree():
+    p = inputs.bf16_problem(768, 512, 4096, seed=6, operand_scale="sqrt_k", bias="f32_normal")
+    outs = {m: gu.host_values(gu.run_bf16(p, out="f32", mode=m, num_sms=0)) for m in MODES}
+    for m in MODES:
+        gu.assert_close(outs[m], outs["dp"], "f32", f"{m} vs dp")
+
+
+# ---- launch hygiene -------------------------------------------------------------------------
+
+def test_repeated_streamk_launches_on_one_stream_are_identical():
+    p = inputs.bf16_problem(512, 512, 2048, seed=8, bias="bf16_uniform")
+    a, b, bias = gu.dev_bf16(p["A"]), gu.dev_bf16(p["B"]), gu.dev_bias(p["bias"])
+    outs = [sk.gemm_bf16(a, b, bias, mode="streamk", num_sms=37) for _ in range(6)]
+    sk.stream_status()
+    first = gu.host_bits(outs[0])
+    for o in outs[1:]:
+        assert np.array_equal(gu.host_bits(o), first)
+    ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "bf16")
+    gu.assert_close(gu.host_values(outs[0]), ref, "bf16")
+
+
+def test_two_streams_run_concurrently_with_separate_workspaces():
+    ps = [inputs.bf16_problem(640, 512, 3072, seed=s, bias="bf16_uniform") for s in (11, 12)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    devs = [(gu.dev_bf16(p["A"]), gu.dev_bf16(p["B"]), gu.dev_bias(p["bias"])) for p in ps]
+    torch.cuda.synchronize()
+    outs = []
+    for _ in range(3):
+        for (a, b, bias), s in zip(devs, streams):
+            with torch.cuda.stream(s):
+                outs.append(sk.gemm_bf16(a, b, bias, mode="streamk", num_sms=60, stream=s))
+    for s in streams:
+        sk.stream_status(s)
+    for i, o in enumerate(outs):
+        p = ps[i % 2]
+        ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "bf16")
+        gu.assert_close(gu.host_values(o), ref, "bf16", f"call {i}")
+
+
+def test_cuda_graph_replay_reuses_the_workspace():
+    # A captured launch keeps one flag epoch; the owners reset consumed flags, so every
+    # replay must still wait for fresh partials.
+    M, N, K = 512, 768, 2048
+    s = torch.cuda.Stream()
+    a = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    b = torch.empty((K, N), dtype=torch.bfloat16, device="cuda")
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    assert sk.sk_workspace_reserve(0, s.cuda_stream, 152) == sk.SK_OK
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        sk.gemm_bf16(a, b, None, out=c, mode="streamk", num_sms=0, stream=s)
+    for seed in (1, 2, 3):
+        p = inputs.bf16_problem(M, N, K, seed=seed, integer=True)
+        a.copy_(gu.dev_bf16(p["A"]))
+        b.copy_(gu.dev_bf16(p["B"]))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert sk.sk_stream_status(s.cuda_stream) == sk.SK_OK
+        want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], None), oracle.BF16)
+        assert np.array_equal(gu.host_bits(c), want)
+
+
+def test_capture_without_reserved_workspace_is_refused():
+    s = torch.cuda.Stream()
+    a = torch.zeros((256, 256), dtype=torch.bfloat16, device="cuda")
+    c = torch.empty((256, 256), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    st = None
+    with torch.cuda.graph(g, stream=s):
+        st = sk.sk_gemm_bf16(a.data_ptr(), a.data_ptr(), None, c.data_ptr(), 1, 256, 256, 256,
+                             0, 2, s.cuda_stream)
+    assert st == sk.SK_ERR_UNSUPPORTED
+
+
+def test_streamk_wait_that_runs_out_reports_timeout():
+    # CTA 1 contributes to tile 1, owned by CTA 0; it is told never to publish its partial.
+    p = inputs.workload("addmm_bf16_256x256x512_f32out")
+    a, b, bias = gu.dev_bf16(p["A"]), gu.dev_bf16(p["B"]), gu.dev_bias(p["bias"])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        sk.gemm_bf16(a, b, bias, out_dtype=torch.float32, mode="streamk", num_sms=3, stream=s,
+                     options={"inject_faults": 1, "drop_release_cta": 1,
+                              "spin_timeout_ns": 20_000_000})
+    assert sk.sk_stream_status(s.cuda_stream) == sk.SK_ERR_TIMEOUT
+    assert sk.sk_stream_status(s.cuda_stream) == sk.SK_OK      # cleared once read
+    c = gu.run_bf16(p, out="f32", mode="streamk", num_sms=3, stream=s)   # recovers
+    ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "f32")
+    gu.assert_close(gu.host_values(c), ref, "f32")
+
+
+# ---- full-size workloads, sampled outputs -------------------------------------------------
+
+def _sampled_check(p, out, modes, num_sms_list=(0,)):
+    ms, ns = gu.sample_positions(p["M"], p["N"])
+    ref = gu.reference(oracle.addmm_bf16_at(p["A"], p["B"], p["bias"], ms, ns), out)
+    a, b, bias = gu.dev_bf16(p["A"]), gu.dev_bf16(p["B"]), gu.dev_bias(p["bias"])
+    for mode in modes:
+        for ns_ in num_sms_list:
+            c = sk.gemm_bf16(a, b, bias, out_dtype=gu.out_torch_dtype(out), mode=mode, num_sms=ns_)
+            sk.stream_status()
+            got = c.float()[torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda()]
+            gu.assert_close(got.cpu().numpy().astype(np.float64), ref, out, f"{mode}/{ns_}")
+            del c
+
+
+def test_addmm_8192_cube_sampled():
+    _sampled_check(inputs.workload("addmm_bf16_8192"), "bf16", MODES)
+
+
+def test_wave_quantised_1920x1920x16384_sampled():
+    _sampled_check(inputs.workload("gemm_bf16_1920x1920x16384"), "bf16", MODES)
+
+
+def test_4096_cube_num_sms_sweep_sampled():
+    _sampled_check(inputs.workload("gemm_bf16_4096"), "bf16", ["persistent", "streamk"],
+                   (1, 16, 32, 64, 128, 0))
+
+
+def test_skinny_64x14336x4096_num_sms_sweep_sampled():
+    _sampled_check(inputs.workload("gemm_bf16_skinny_64x14336x4096"), "bf16",
+                   ["dp", "persistent", "streamk", "hybrid"], (1, 16, 32, 64, 128, 0))
