@@ -137,6 +137,28 @@ sk_status_t sk_gemm_mxfp4_ex(const void* A, const void* A_scale, const void* B,
                              sk_mode_t mode, const sk_options_t* options, void* stream);
 
 /*
+ * sk_gemm_bf16_static — sk_gemm_bf16 for callers that cannot allocate device memory.
+ * The pages this library follows have no counterpart to this entry point.
+ * Some callers may not allocate at the point where they run the GEMM (they live under an
+ * allocator they do not own, sit on a path where an allocation could synchronise the device,
+ * or must not fail for lack of memory after start-up).  This entry point allocates nothing:
+ * its scratch (error words, Stream-K flags and up to 160 partial tiles of 128 x 128 fp32,
+ * about 10 MiB) is one fixed array inside the library that every GPU loading the library
+ * keeps until the process exits.  Arguments and results are those of sk_gemm_bf16; it
+ * always uses 128 x 128 CTA tiles.
+ *   - Returns SK_ERR_UNSUPPORTED when the schedule would need more than 160 Stream-K slots.
+ *   - The first call on a device looks up the array's device address and prepares the kernel
+ *     on that device; make that first call before any stream capture on the device.
+ *   - All calls share the one array (it keeps the last call's contents; each call clears the
+ *     parts that must start at zero on its stream).  Calls that overlap on the GPU race and
+ *     give wrong results: serialise them.
+ *   - Kernel-side timeouts of this entry point are not reported by sk_stream_status.
+ */
+sk_status_t sk_gemm_bf16_static(const void* A, const void* B, const void* bias, void* C,
+                                sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K,
+                                int num_sms, sk_mode_t mode, void* stream);
+
+/*
  * sk_stream_status — waits for `stream`, then returns (and clears) the first error the kernels
  * recorded in that stream's workspace on the current device: SK_OK, SK_ERR_TIMEOUT, or
  * SK_ERR_CUDA if the stream itself reports a CUDA error.

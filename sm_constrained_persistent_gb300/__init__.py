@@ -73,6 +73,8 @@ def lib():
             h.sk_gemm_mxfp4_ex.restype = i32
             h.sk_gemm_mxfp4_ex.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, i32, i32,
                                            ctypes.POINTER(Options), vp]
+            h.sk_gemm_bf16_static.restype = i32
+            h.sk_gemm_bf16_static.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, i32, vp]
             h.sk_stream_status.restype = i32
             h.sk_stream_status.argtypes = [vp]
             h.sk_workspace_reserve.restype = i32
@@ -122,6 +124,12 @@ def sk_gemm_mxfp4_ex(A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sm
                      options, stream):
     return lib().sk_gemm_mxfp4_ex(A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sms,
                                   mode, _opts(options), stream)
+
+
+def sk_gemm_bf16_static(A, B, bias, C, out_dtype, M, N, K, num_sms, mode, stream):
+    """The bf16 addmm that allocates nothing (scratch in a fixed array inside the library),
+    for callers that may not allocate device memory; calls must not overlap on the GPU."""
+    return lib().sk_gemm_bf16_static(A, B, bias, C, out_dtype, M, N, K, num_sms, mode, stream)
 
 
 def sk_stream_status(stream):
