@@ -15,10 +15,17 @@
 // tritonBLAS PR #74 "Stream-k mxfp4 kernel"), and an owner's split tile is its last Stream-K
 // piece, continued by CTAs c+1, c+2, ...
 //
-// Linear tile index -> (tile row, tile column) uses a grouped raster: groups of `group_m`
-// tile rows, column-major inside a group, so CTAs running at the same time share operand
-// panels in L2.  The raster changes only the fp32 summation grouping of nothing: every tile
-// is still summed over k in ascending order.
+// Linear tile index -> (tile row, tile column) goes through two bijections:
+//  1. In the Stream-K region, the tau-th tile owned by CTA c is given raster position
+//     whole_tiles + tau * g + c (the CTAs holding one more tile than the others come last, in
+//     CTA order).  CTAs advance through their owned tiles in step, so the tiles they work on at
+//     the same time take consecutive raster positions -- one compact block, as in a wave of the
+//     persistent schedule -- instead of being spread over the whole matrix.  The whole-tile
+//     region keeps its linear order.
+//  2. A grouped raster: groups of `group_m` tile rows, column-major inside a group, so tiles
+//     at consecutive raster positions share A and B panels in L2.
+// Both only decide which output tile a piece works on; every tile is still summed over k in
+// ascending order.
 #pragma once
 
 #include <cstdint>
@@ -89,14 +96,35 @@ struct Cursor {
   }
 };
 
+// Raster position of a linear tile (bijection 1 above).
+__host__ __device__ __forceinline__ int64_t raster_position(const Plan& p, int64_t t) {
+  if (t < p.whole_tiles) return t;
+  const int64_t local = t - p.whole_tiles;
+  const int64_t x = local * p.iters;                       // its k = 0 iteration
+  const int64_t long_span = p.sk_extra * (p.sk_base + 1);  // iterations of the longer ranges
+  int64_t c;                                               // owner: the CTA whose range holds x
+  if (x < long_span) {
+    c = x / (p.sk_base + 1);
+  } else {
+    c = p.sk_base > 0 ? p.sk_extra + (x - long_span) / p.sk_base : p.sk_extra;
+  }
+  const int64_t start = sk_range_begin(p, c);
+  const int64_t first_owned = (start + p.iters - 1) / p.iters;   // first tile whose k = 0 is c's
+  const int64_t tau = local - first_owned;
+  const int64_t f = p.sk_base / p.iters;   // every CTA owns f or f + 1 tiles
+  const int64_t pos = (tau < f) ? tau * p.grid + c : f * p.grid + (first_owned - c * f);
+  return p.whole_tiles + pos;
+}
+
 __host__ __device__ __forceinline__ void tile_coords(const Plan& p, int64_t t, int32_t& tm,
                                                      int32_t& tn) {
+  const int64_t r_pos = raster_position(p, t);
   const int64_t per_group = static_cast<int64_t>(p.group_m) * p.tiles_n;
-  const int64_t group = t / per_group;
+  const int64_t group = r_pos / per_group;
   const int64_t first_m = group * p.group_m;
   const int64_t rows_here =
       (p.tiles_m - first_m < p.group_m) ? (p.tiles_m - first_m) : p.group_m;
-  const int64_t r = t - group * per_group;
+  const int64_t r = r_pos - group * per_group;
   tm = static_cast<int32_t>(first_m + r % rows_here);
   tn = static_cast<int32_t>(r / rows_here);
 }

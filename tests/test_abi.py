@@ -133,14 +133,45 @@ def test_kernel_scheduler_matches_oracle_restatement(lib, mode, shape, g):
     _same_split(mode, M, N, K, g, 148, 128)
 
 
-def test_raster_is_a_bijection_onto_the_tile_grid(lib):
-    for (M, N, group) in [(8192, 8192, 16), (1920, 1920, 16), (1000, 3000, 5), (128, 256, 1),
-                          (640, 128, 3)]:
-        plan = sk.sk_plan(0, M, N, 64, 0, "dp", 148, {"tile_n": 128, "raster_group": group})
-        segs = sk.sk_plan_segments(plan)
-        cells = set(map(tuple, segs[:, 5:7].tolist()))
-        assert len(cells) == plan.tiles
-        assert cells == {(i, j) for i in range(plan.tiles_m) for j in range(plan.tiles_n)}
+@pytest.mark.parametrize("mode", ["dp", "persistent", "streamk", "hybrid"])
+@pytest.mark.parametrize("M,N,K,group,g", [(8192, 8192, 8192, 16, 152), (1920, 1920, 16384, 16, 152),
+                                           (1000, 3000, 640, 5, 37), (128, 256, 64, 1, 3),
+                                           (640, 128, 4096, 3, 7), (256, 256, 512, 16, 3),
+                                           (2048, 512, 128, 4, 148)])
+def test_raster_is_a_bijection_onto_the_tile_grid(lib, mode, M, N, K, group, g):
+    plan = sk.sk_plan(0, M, N, K, g, mode, 152, {"tile_n": 128, "raster_group": group})
+    segs = sk.sk_plan_segments(plan)
+    owned = segs[segs[:, 2] == 0]          # the piece holding k = 0 of each tile
+    cells = list(map(tuple, owned[:, 5:7].tolist()))
+    assert len(cells) == plan.tiles == len(set(cells))
+    assert set(cells) == {(i, j) for i in range(plan.tiles_m) for j in range(plan.tiles_n)}
+    # every piece of a tile maps to the same cell
+    cell_of = {int(t): (int(a), int(b)) for t, a, b in owned[:, [1, 5, 6]].tolist()}
+    for t, a, b in segs[:, [1, 5, 6]].tolist():
+        assert cell_of[t] == (a, b)
+
+
+def _raster_pos(plan, tm, tn):
+    group = tm // plan.raster_group
+    first = group * plan.raster_group
+    rows = min(plan.tiles_m - first, plan.raster_group)
+    return first * plan.tiles_n + tn * rows + (tm - first)
+
+
+@pytest.mark.parametrize("M,N,K,g", [(8192, 8192, 8192, 152), (4096, 4096, 4096, 152),
+                                     (1920, 1920, 16384, 152), (3000, 2000, 1000, 37)])
+def test_streamk_tiles_worked_on_together_form_one_raster_block(lib, M, N, K, g):
+    plan = sk.sk_plan(0, M, N, K, g, "streamk", 152, {"tile_n": 128})
+    segs = sk.sk_plan_segments(plan)
+    f = plan.sk_base // plan.iters
+    for cta in range(plan.grid):
+        mine = segs[(segs[:, 0] == cta) & (segs[:, 2] == 0)]
+        for tau, row in enumerate(mine.tolist()):
+            pos = _raster_pos(plan, row[5], row[6]) - plan.whole_tiles
+            if tau < f:
+                assert pos == tau * plan.grid + cta
+            else:
+                assert f * plan.grid <= pos < plan.tiles - plan.whole_tiles
 
 
 def test_streamk_256_cube_split_matches_golden(lib):
