@@ -118,6 +118,10 @@ sk_status_t sk_gemm_mxfp4(const void* A, const void* A_scale, const void* B,
  *                         passed with inject_faults = 0) = off.  When inject_faults != 0, the
  *                         CTA with this index never releases its Stream-K partial, so its
  *                         tile's owner times out.
+ *   tile_m:               0 = automatic, 128 = one CTA per tile, 256 = a 2-CTA cluster (an SM
+ *                         pair) per 256 x 256 tile.  Pair tiles need tile_n 0 or 256 and at
+ *                         least two SMs; num_sms then counts both SMs of every pair (an odd
+ *                         num_sms leaves one SM unused).
  */
 typedef struct {
   int32_t tile_n;
@@ -125,6 +129,8 @@ typedef struct {
   int64_t spin_timeout_ns;
   int32_t inject_faults;
   int32_t drop_release_cta;
+  int32_t tile_m;
+  int32_t reserved;
 } sk_options_t;
 
 sk_status_t sk_gemm_bf16_ex(const void* A, const void* B, const void* bias, void* C,
@@ -180,6 +186,22 @@ void sk_workspace_release_all(void);
 const char* sk_status_string(sk_status_t status);
 
 /*
+ * sk_device_caps — what the library can launch on `device` (prepares every kernel variant on
+ * it): SM count, compute capability, resident CTAs per SM of the one-CTA-per-tile variants
+ * (bf16 128x128, bf16 128x256, MXFP4 128x128) and resident 2-CTA clusters of the SM-pair
+ * variants (bf16 and MXFP4 256x256), with the CUDA error (0 = none) of each variant's set-up.
+ */
+typedef struct {
+  int32_t sm_count;
+  int32_t cc_major, cc_minor;
+  int32_t ctas_per_sm[3];        /* bf16 128x128, bf16 128x256, MXFP4 128x128   */
+  int32_t max_pair_clusters[2];  /* bf16 256x256 pairs, MXFP4 256x256 pairs      */
+  int32_t setup_error[5];        /* cudaError_t of each variant's set-up, in the order above */
+} sk_device_caps_t;
+
+sk_status_t sk_device_caps(int device, sk_device_caps_t* caps);
+
+/*
  * Planning (host only, makes no CUDA call).  Fills *plan with the schedule the library would
  * launch for this problem on a device with `sm_count` SMs.  format: 0 = bf16, 1 = MXFP4.
  */
@@ -190,9 +212,9 @@ typedef struct {
   int32_t tiles_m, tiles_n;
   int64_t tiles;                    /* tiles_m * tiles_n                                  */
   int32_t iters;                    /* k-iterations per tile                              */
-  int32_t grid;                     /* CTAs launched                                      */
+  int32_t grid;                     /* scheduling units: CTAs, or CTA pairs (see below)   */
   int32_t raster_group;
-  int32_t reserved;
+  int32_t ctas_per_tile;            /* 1, or 2 for SM-pair tiles (2 * grid CTAs launched) */
   int64_t whole_tiles;              /* linear tiles [0, whole_tiles) run whole            */
   int64_t sk_tiles;                 /* linear tiles [whole_tiles, tiles) run Stream-K     */
   int64_t sk_base;                  /* Stream-K iterations per CTA ...                    */
@@ -203,8 +225,9 @@ sk_status_t sk_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, sk
                     int sm_count, const sk_options_t* options, sk_plan_t* plan);
 
 /*
- * Enumerates the work the kernel's CTAs perform for `plan`, in each CTA's execution order:
- * rows of 7 int64 (cta, linear tile, k_begin, k_end, role, tile_m index, tile_n index), role
+ * Enumerates the work the kernel's CTAs (or CTA pairs) perform for `plan`, in each one's
+ * execution order: rows of 7 int64 (unit, linear tile, k_begin, k_end, role, tile_m index,
+ * tile_n index), role
  * 0 = whole tile, 1 = owner of a split tile, 2 = partial contribution.  Writes at most `cap`
  * rows and returns the total count (call with cap = 0 to size the buffer), or -1 on bad input.
  * This runs the same scheduling code the kernel runs.

@@ -35,7 +35,8 @@ class Options(ctypes.Structure):
     """sk_options_t."""
     _fields_ = [("tile_n", ctypes.c_int32), ("raster_group", ctypes.c_int32),
                 ("spin_timeout_ns", ctypes.c_int64), ("inject_faults", ctypes.c_int32),
-                ("drop_release_cta", ctypes.c_int32)]
+                ("drop_release_cta", ctypes.c_int32), ("tile_m", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):
@@ -44,9 +45,16 @@ class Plan(ctypes.Structure):
                 ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("tile_k", ctypes.c_int32),
                 ("tiles_m", ctypes.c_int32), ("tiles_n", ctypes.c_int32),
                 ("tiles", ctypes.c_int64), ("iters", ctypes.c_int32), ("grid", ctypes.c_int32),
-                ("raster_group", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("raster_group", ctypes.c_int32), ("ctas_per_tile", ctypes.c_int32),
                 ("whole_tiles", ctypes.c_int64), ("sk_tiles", ctypes.c_int64),
                 ("sk_base", ctypes.c_int64), ("sk_extra", ctypes.c_int64)]
+
+
+class DeviceCaps(ctypes.Structure):
+    """sk_device_caps_t."""
+    _fields_ = [("sm_count", ctypes.c_int32), ("cc_major", ctypes.c_int32),
+                ("cc_minor", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32 * 3),
+                ("max_pair_clusters", ctypes.c_int32 * 2), ("setup_error", ctypes.c_int32 * 5)]
 
 
 def library_path() -> str:
@@ -86,6 +94,8 @@ def lib():
             h.sk_plan.restype = i32
             h.sk_plan.argtypes = [i32, i64, i64, i64, i32, i32, i32, ctypes.POINTER(Options),
                                   ctypes.POINTER(Plan)]
+            h.sk_device_caps.restype = i32
+            h.sk_device_caps.argtypes = [i32, ctypes.POINTER(DeviceCaps)]
             h.sk_plan_segments.restype = i64
             h.sk_plan_segments.argtypes = [ctypes.POINTER(Plan), vp, i64]
             _handle = h
@@ -146,6 +156,17 @@ def sk_workspace_release_all():
 
 def sk_status_string(status):
     return lib().sk_status_string(status).decode()
+
+
+def sk_device_caps(device=0):
+    """dict of the device's SM count, compute capability and per-variant capacities."""
+    c = DeviceCaps()
+    st = lib().sk_device_caps(device, ctypes.byref(c))
+    if st != SK_OK:
+        raise SkError(st, "sk_device_caps")
+    return {"sm_count": c.sm_count, "cc": (c.cc_major, c.cc_minor),
+            "ctas_per_sm": list(c.ctas_per_sm), "max_pair_clusters": list(c.max_pair_clusters),
+            "setup_error": list(c.setup_error)}
 
 
 def sk_plan(fmt, M, N, K, num_sms, mode, sm_count, options=None):

@@ -29,45 +29,71 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// max_pairs: how many 2-CTA clusters the device can hold at once (the planner's caller passes
+// sm_count / 2 when it cannot ask the device).
 sk_status_t make_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, int mode,
-                      int sm_count, const sk_options_t* opt, sk_plan_t* p) {
+                      int sm_count, int max_pairs, const sk_options_t* opt, sk_plan_t* p) {
   if (p == nullptr || (format != 0 && format != 1) || mode < 0 || mode > 3 || sm_count < 1)
     return SK_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return SK_ERR_INVALID_ARG;
   int tile_n = opt ? opt->tile_n : 0;
+  int tile_m = opt ? opt->tile_m : 0;
   if (tile_n != 0 && tile_n != 128 && tile_n != 256) return SK_ERR_INVALID_ARG;
-  if (format == 1 && tile_n == 256) return SK_ERR_INVALID_ARG;
-  if (tile_n == 0) {
-    if (format == 1) {
-      tile_n = 128;
-    } else {
-      // Wide tiles halve the B traffic per FLOP; use them while they still fill every SM.
-      const int64_t wide_tiles = ceil_div(M, kTileM) * ceil_div(N, 256);
-      tile_n = (N >= 256 && wide_tiles >= sm_count) ? 256 : 128;
+  if (tile_m != 0 && tile_m != 128 && tile_m != 256) return SK_ERR_INVALID_ARG;
+  if (tile_m == 256 && tile_n == 128) return SK_ERR_INVALID_ARG;
+  if (format == 1 && tile_m != 256 && tile_n == 256) return SK_ERR_INVALID_ARG;
+  const int64_t sms = (num_sms <= 0 || num_sms > sm_count) ? sm_count : num_sms;
+  const int64_t pairs_avail = std::min<int64_t>(sms / 2, max_pairs);
+  const int64_t pair_tiles = ceil_div(M, 256) * ceil_div(N, 256);
+  bool pair;
+  if (tile_m == 256) {
+    if (pairs_avail < 1) return SK_ERR_INVALID_ARG;
+    pair = true;
+  } else if (tile_m == 128 || tile_n == 128) {
+    pair = false;
+  } else {
+    // SM pairs halve the operand bytes per FLOP; use them when the tile still has more than
+    // 128 real rows, there are at least two tiles, and at least two pairs to run them.
+    pair = M > 128 && pair_tiles >= 2 && pairs_avail >= 2;
+  }
+  if (pair) {
+    tile_m = 256;
+    tile_n = 256;
+  } else {
+    tile_m = kTileM;
+    if (tile_n == 0) {
+      if (format == 1) {
+        tile_n = 128;
+      } else {
+        // Wide tiles halve the B traffic per FLOP; use them while they still fill every SM.
+        const int64_t wide_tiles = ceil_div(M, kTileM) * ceil_div(N, 256);
+        tile_n = (N >= 256 && wide_tiles >= sm_count) ? 256 : 128;
+      }
     }
   }
   std::memset(p, 0, sizeof(*p));
   p->format = format;
   p->mode = mode;
-  p->tile_m = kTileM;
+  p->tile_m = tile_m;
   p->tile_n = tile_n;
   p->tile_k = format == 1 ? kMxTileK : kBf16TileK;
-  const int64_t tiles_m = ceil_div(M, kTileM), tiles_n = ceil_div(N, tile_n);
+  p->ctas_per_tile = pair ? 2 : 1;
+  const int64_t tiles_m = ceil_div(M, tile_m), tiles_n = ceil_div(N, tile_n);
   const int64_t tiles = tiles_m * tiles_n;
   const int64_t iters = ceil_div(K, p->tile_k);
-  if (tiles > kMaxDim) return SK_ERR_UNSUPPORTED;
+  if (tiles > kMaxDim / 2) return SK_ERR_UNSUPPORTED;
   p->tiles_m = static_cast<int32_t>(tiles_m);
   p->tiles_n = static_cast<int32_t>(tiles_n);
   p->tiles = tiles;
   p->iters = static_cast<int32_t>(iters);
-  const int64_t sms = (num_sms <= 0 || num_sms > sm_count) ? sm_count : num_sms;
+  const int64_t units = pair ? pairs_avail : sms;   // schedulable workers
   int64_t grid = 0, sk_tiles = 0;
   switch (mode) {
     case SK_MODE_DP: grid = tiles; sk_tiles = 0; break;
-    case SK_MODE_PERSISTENT: grid = std::min(sms, tiles); sk_tiles = 0; break;
-    case SK_MODE_STREAMK: grid = std::min(sms, tiles * iters); sk_tiles = tiles; break;
-    default: grid = std::min(sms, tiles * iters); sk_tiles = tiles % grid; break;
+    case SK_MODE_PERSISTENT: grid = std::min(units, tiles); sk_tiles = 0; break;
+    case SK_MODE_STREAMK: grid = std::min(units, tiles * iters); sk_tiles = tiles; break;
+    default: grid = std::min(units, tiles * iters); sk_tiles = tiles % grid; break;
   }
   p->grid = static_cast<int32_t>(grid);
   p->whole_tiles = tiles - sk_tiles;
@@ -75,6 +101,7 @@ sk_status_t make_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, 
   p->sk_base = sk_tiles * iters / grid;
   p->sk_extra = sk_tiles * iters % grid;
   int group = opt && opt->raster_group > 0 ? opt->raster_group : kDefaultRasterGroup;
+  if (pair && !(opt && opt->raster_group > 0)) group = kDefaultRasterGroup / 2;
   p->raster_group = static_cast<int32_t>(std::min<int64_t>(group, tiles_m));
   return SK_OK;
 }
@@ -104,7 +131,9 @@ struct DeviceInfo {
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
   bool variant_ready[sk::kNumVariants] = {};
-  int ctas_per_sm[sk::kNumVariants] = {};
+  int ctas_per_sm[sk::kNumVariants] = {};   // 1-CTA variants: resident CTAs per SM
+  int max_pairs[sk::kNumVariants] = {};     // pair variants: resident 2-CTA clusters
+  int setup_error[sk::kNumVariants] = {};   // cudaError_t of the variant's last set-up
 };
 
 struct Workspace {
@@ -173,8 +202,18 @@ sk_status_t device_info(int dev, DeviceInfo** out) {
 sk_status_t ensure_variant(DeviceInfo& d, int variant) {
   if (!d.variant_ready[variant]) {
     int n = 0;
-    if (sk::variant_setup(variant, &n) != cudaSuccess) return SK_ERR_CUDA;
-    d.ctas_per_sm[variant] = n;
+    const cudaError_t e = sk::variant_is_pair(variant) ? sk::pair_variant_setup(variant, &n)
+                                                       : sk::variant_setup(variant, &n);
+    d.setup_error[variant] = static_cast<int>(e);
+    if (e != cudaSuccess) {
+      cudaGetLastError();   // clear the sticky-free launch error so later calls can run
+      return SK_ERR_CUDA;
+    }
+    if (sk::variant_is_pair(variant)) {
+      d.max_pairs[variant] = n;
+    } else {
+      d.ctas_per_sm[variant] = n;
+    }
     d.variant_ready[variant] = true;
   }
   return SK_OK;
@@ -234,9 +273,23 @@ struct MxLayout {
 MxLayout mx_layout(const sk_plan_t& p) {
   MxLayout l;
   l.kgroups = 2 * static_cast<int64_t>(p.iters);
-  l.a_row_blocks = p.tiles_m;
+  l.a_row_blocks = static_cast<int64_t>(p.tiles_m) * (p.tile_m / 128);
   l.b_row_blocks = static_cast<int64_t>(p.tiles_n) * (p.tile_n / 128);
   return l;
+}
+
+// The rearranged scales as a 2-D uint32 tensor of 1 KB rows: row (row block, k-iteration)
+// holds the two 512-byte k groups one stage of the pair kernel reads.
+bool encode_scale_rows(CUtensorMap* map, const void* base, int64_t row_blocks, int64_t iters) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {256, static_cast<cuuint64_t>(row_blocks * iters)};
+  const cuuint64_t strides[1] = {1024};
+  const cuuint32_t box[2] = {256, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -261,7 +314,9 @@ sk_status_t validate(int format, const void* A, const void* A_scale, const void*
   }
   if (opt != nullptr) {
     if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256) return SK_ERR_INVALID_ARG;
-    if (format == 1 && opt->tile_n == 256) return SK_ERR_INVALID_ARG;
+    if (opt->tile_m != 0 && opt->tile_m != 128 && opt->tile_m != 256) return SK_ERR_INVALID_ARG;
+    if (opt->tile_m == 256 && opt->tile_n == 128) return SK_ERR_INVALID_ARG;
+    if (format == 1 && opt->tile_n == 256 && opt->tile_m != 256) return SK_ERR_INVALID_ARG;
     if (opt->spin_timeout_ns < 0 || opt->raster_group < 0) return SK_ERR_INVALID_ARG;
   }
   return SK_OK;
@@ -282,41 +337,56 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   if ((st = device_info(dev, &di)) != SK_OK) return st;
   if (di->cc_major != 10 || di->cc_minor != 3) return SK_ERR_UNSUPPORTED;   // built for sm_103a
 
+  // The pair variants' cluster capacity is needed to plan; set both candidates up first.
+  const int pair_variant = format == 1 ? sk::kVariantMxPair : sk::kVariantBf16Pair;
+  if ((st = ensure_variant(*di, pair_variant)) != SK_OK) return st;
   sk_plan_t plan;
-  if ((st = make_plan(format, M, N, K, num_sms, mode, di->sm_count, opt, &plan)) != SK_OK) return st;
-  const int variant = format == 1 ? sk::kVariantMxN128
-                                  : (plan.tile_n == 256 ? sk::kVariantBf16N256 : sk::kVariantBf16N128);
+  if ((st = make_plan(format, M, N, K, num_sms, mode, di->sm_count, di->max_pairs[pair_variant],
+                      opt, &plan)) != SK_OK)
+    return st;
+  const bool pair = plan.ctas_per_tile == 2;
+  const int variant = pair ? pair_variant
+                           : (format == 1 ? sk::kVariantMxN128
+                                          : (plan.tile_n == 256 ? sk::kVariantBf16N256
+                                                                : sk::kVariantBf16N128));
   if ((st = ensure_variant(*di, variant)) != SK_OK) return st;
   const bool streamk = plan.sk_tiles > 0;
-  if (streamk && static_cast<int64_t>(plan.grid) >
-                     static_cast<int64_t>(di->ctas_per_sm[variant]) * di->sm_count)
-    return SK_ERR_NOT_CORESIDENT;
+  if (streamk) {
+    const int64_t capacity = pair ? di->max_pairs[variant]
+                                  : static_cast<int64_t>(di->ctas_per_sm[variant]) * di->sm_count;
+    if (plan.grid > capacity) return SK_ERR_NOT_CORESIDENT;
+  }
+  const int64_t ctas = static_cast<int64_t>(plan.grid) * plan.ctas_per_tile;
 
-  const size_t P_bytes = streamk ? static_cast<size_t>(plan.grid) * kTileM * plan.tile_n * sizeof(float) : 0;
+  const size_t P_bytes = streamk ? static_cast<size_t>(ctas) * kTileM * plan.tile_n * sizeof(float) : 0;
   const MxLayout mx = mx_layout(plan);
   Workspace* ws = nullptr;
-  if ((st = ensure_workspace(dev, stream, P_bytes, static_cast<size_t>(plan.grid),
+  if ((st = ensure_workspace(dev, stream, P_bytes, static_cast<size_t>(ctas),
                              format == 1 ? mx.bytes() : 0, &ws)) != SK_OK)
     return st;
   if (++ws->epoch == 0) ws->epoch = 1;
 
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmSfa, tmSfb;
+  std::memset(&tmSfa, 0, sizeof(tmSfa));
+  std::memset(&tmSfb, 0, sizeof(tmSfb));
+  const uint32_t b_box = pair ? 128u : static_cast<uint32_t>(plan.tile_n);   // B rows per CTA (MXFP4)
   bool ok;
   if (format == 0) {
     ok = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, M, K, 64, kTileM) &&
          encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, 64, 64);
   } else {
     ok = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, M, K / 2, 128, kTileM) &&
-         encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, N, K / 2, 128,
-                   static_cast<uint32_t>(plan.tile_n));
+         encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, N, K / 2, 128, b_box);
   }
   if (!ok) return SK_ERR_CUDA;
 
   sk::Launch l = {};
   l.tmA = &tmA;
   l.tmB = &tmB;
-  l.grid = plan.grid;
-  l.cooperative = streamk;
+  l.tmSfa = &tmSfa;
+  l.tmSfb = &tmSfb;
+  l.grid = static_cast<int>(ctas);
+  l.cooperative = streamk && !pair;
   l.stream = stream;
   sk::Args& a = l.args;
   a.bias = bias;
@@ -345,8 +415,11 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
     a.sfa = sfa;
     a.sfb = sfb;
     a.sf_kgroups = mx.kgroups;
+    if (pair && !(encode_scale_rows(&tmSfa, sfa, mx.a_row_blocks, plan.iters) &&
+                  encode_scale_rows(&tmSfb, sfb, mx.b_row_blocks, plan.iters)))
+      return SK_ERR_CUDA;
   }
-  cudaError_t e = sk::variant_launch(variant, l);
+  cudaError_t e = pair ? sk::pair_variant_launch(variant, l) : sk::variant_launch(variant, l);
   if (e == cudaErrorCooperativeLaunchTooLarge) return SK_ERR_NOT_CORESIDENT;
   return e == cudaSuccess ? SK_OK : SK_ERR_CUDA;
 }
@@ -421,8 +494,14 @@ sk_status_t sk_workspace_reserve(int device, void* stream_ptr, int max_grid, int
     size_t sf_bytes = 0;
     if (max_mx_m > 0 && max_mx_n > 0 && max_mx_k > 0) {
       sk_plan_t p;
-      st = make_plan(1, max_mx_m, max_mx_n, max_mx_k, 0, SK_MODE_DP, 1, nullptr, &p);
+      // the larger of the two tile layouts
+      sk_options_t o = {};
+      o.tile_m = 128;
+      st = make_plan(1, max_mx_m, max_mx_n, max_mx_k, 0, SK_MODE_DP, 1, 0, &o, &p);
       if (st == SK_OK) sf_bytes = mx_layout(p).bytes();
+      o.tile_m = 256;
+      if (st == SK_OK && make_plan(1, max_mx_m, max_mx_n, max_mx_k, 0, SK_MODE_DP, 2, 1, &o, &p) == SK_OK)
+        sf_bytes = std::max(sf_bytes, mx_layout(p).bytes());
     }
     Workspace* ws = nullptr;
     if (st == SK_OK)
@@ -464,9 +543,41 @@ const char* sk_status_string(sk_status_t s) {
   return "unknown status";
 }
 
+sk_status_t sk_device_caps(int device, sk_device_caps_t* caps) {
+  if (caps == nullptr) return SK_ERR_INVALID_ARG;
+  std::memset(caps, 0, sizeof(*caps));
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return SK_ERR_UNSUPPORTED;
+  if (cudaSetDevice(device) != cudaSuccess) return SK_ERR_INVALID_ARG;
+  sk_status_t st = SK_OK;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo* d = nullptr;
+    st = device_info(device, &d);
+    if (st == SK_OK) {
+      caps->sm_count = d->sm_count;
+      caps->cc_major = d->cc_major;
+      caps->cc_minor = d->cc_minor;
+      if (d->cc_major == 10 && d->cc_minor == 3) {
+        for (int v = 0; v < sk::kNumVariants; ++v) ensure_variant(*d, v);
+        caps->ctas_per_sm[0] = d->ctas_per_sm[sk::kVariantBf16N128];
+        caps->ctas_per_sm[1] = d->ctas_per_sm[sk::kVariantBf16N256];
+        caps->ctas_per_sm[2] = d->ctas_per_sm[sk::kVariantMxN128];
+        caps->max_pair_clusters[0] = d->max_pairs[sk::kVariantBf16Pair];
+        caps->max_pair_clusters[1] = d->max_pairs[sk::kVariantMxPair];
+        for (int v = 0; v < sk::kNumVariants; ++v) caps->setup_error[v] = d->setup_error[v];
+      } else {
+        st = SK_ERR_UNSUPPORTED;
+      }
+    }
+  }
+  cudaSetDevice(prev);
+  return st;
+}
+
 sk_status_t sk_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, sk_mode_t mode,
                     int sm_count, const sk_options_t* options, sk_plan_t* plan) {
-  return make_plan(format, M, N, K, num_sms, mode, sm_count, options, plan);
+  return make_plan(format, M, N, K, num_sms, mode, sm_count, sm_count / 2, options, plan);
 }
 
 int64_t sk_plan_segments(const sk_plan_t* plan, int64_t* rows, int64_t cap) {

@@ -1,0 +1,468 @@
+// The addmm GEMM kernel on SM pairs: a cluster of two CTAs computes one 256 x 256 output tile
+// with tcgen05 cta_group::2 MMAs (M = 256), each CTA holding 128 rows x 256 fp32 columns of
+// the accumulator in its own tensor memory.  Same schedules, roles and results as
+// sk_kernel.cuh; what changes is the data each SM moves per FLOP: a CTA loads its 128 rows of A
+// and half (128 columns) of the B tile, and the pair's MMA reads the other half of B from the
+// peer CTA, so operand traffic per SM per MMA drops by a third (bf16) to a half (MXFP4).
+//
+// Roles (320 threads per CTA, one CTA per SM, clusters of 2):
+//   warp 0      TMA producer of this CTA's halves.  Both CTAs' loads complete on the leader
+//               CTA's (cluster rank 0) "full" barrier, which expects the bytes of both.
+//   warp 1      both CTAs allocate tensor memory together; in the leader one lane issues the
+//               cta_group::2 MMAs and commits them to the "empty" and "accumulator full"
+//               barriers of both CTAs at once (multicast).
+//   warps 2..9  epilogue, two warps per 32-lane quarter: warp w reads lanes 32*(w%4).. and
+//               columns [128*h, 128*h+128), h = (w-2)/4.  Each thread first drains its 128
+//               accumulator columns into registers and releases the accumulator to the
+//               leader, then spills (contribution) or aggregates + bias + casts + stores.
+// MXFP4 keeps one accumulator (256 columns) so that the per-stage scale-factor slots fit in
+// the 512 tensor-memory columns; the fast drain keeps the MMA's wait for it short.  bf16 keeps
+// two accumulators.
+#pragma once
+
+#include "sk_kernel.cuh"
+
+namespace sk {
+
+constexpr int kPairThreads = 320;
+constexpr int kPairEpilogueThreads = 256;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_addr(p)), "r"(rank));
+  return out;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(dst)),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem,
+                                              uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], "
+      "[%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_copy_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Arrive once on `bar` (same offset) in both CTAs of the pair when this thread's tcgen05
+// operations have completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_addr(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+// Arrive once on this CTA's `bar` when this thread's tcgen05 operations have completed.
+__device__ __forceinline__ void mma_commit_pair_local(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_addr(bar))
+               : "memory");
+}
+
+// TMA 2-D load into this CTA's shared memory, completing on a barrier of either CTA of the
+// pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t cluster_bar, int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+template <bool kMx>
+struct PairCfg {
+  static constexpr int kBN = 256;                        // pair tile: 256 x 256
+  static constexpr int kHalfN = kBN / 2;                 // B columns loaded by each CTA
+  static constexpr int kTileK = kMx ? 256 : 64;
+  static constexpr int kMmaK = kMx ? 64 : 16;
+  static constexpr int kMmasPerStage = kTileK / kMmaK;   // 4
+  static constexpr int kStageA = kBM * 128;              // 16 KB
+  static constexpr int kStageB = kHalfN * 128;           // 16 KB
+  static constexpr int kStageSfa = kMx ? 1024 : 0;       // own 128 rows, 2 k groups
+  static constexpr int kStageSfb = kMx ? 2048 : 0;       // all 256 columns, 2 k groups
+  static constexpr int kStageBytes = kStageA + kStageB + kStageSfa + kStageSfb;
+  static constexpr int kStages = (212 * 1024) / kStageBytes;
+  static constexpr int kAccBufs = kMx ? 1 : 2;
+  static constexpr uint32_t kAccCols = kBN;
+  static constexpr uint32_t kSfaCols = 8;
+  static constexpr uint32_t kSfbCols = 16;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kAccBufs * kAccCols + (kMx ? kStages * (kSfaCols + kSfbCols) : 0) <= kTmemCols,
+                "tensor memory budget");
+  static constexpr int kBarrierBytes = 256;
+  static constexpr size_t kSmemBytes =
+      1024 + static_cast<size_t>(kStages) * kStageBytes + kBarrierBytes;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static constexpr uint32_t kIdesc =
+      kMx ? ((1u << 7) | (1u << 10) | (1u << 23) | (uint32_t(kBN >> 3) << 17) |
+             (uint32_t(256 >> 4) << 24))
+          : ((1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | (uint32_t(kBN >> 3) << 17) |
+             (uint32_t(256 >> 4) << 24));
+};
+
+// Registers are granted per 128-thread warpgroup, so 320 threads are charged as 384: the
+// launch bound caps the kernel at 65536 / 384 -> 168 registers per thread.
+template <bool kMx>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmSfa,
+                     const __grid_constant__ CUtensorMap tmSfb, const __grid_constant__ Args args) {
+  using Cf = PairCfg<kMx>;
+  constexpr int S = Cf::kStages;
+  constexpr int kBN = Cf::kBN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* ring_a = smem;
+  uint8_t* ring_b = ring_a + S * Cf::kStageA;
+  uint8_t* ring_sfa = ring_b + S * Cf::kStageB;
+  uint8_t* ring_sfb = ring_sfa + S * Cf::kStageSfa;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring_sfb + S * Cf::kStageSfb);
+  uint64_t* full = bars;                 // leader: both CTAs' bytes of a stage
+  uint64_t* empty = bars + S;            // each CTA: its stage may be refilled
+  uint64_t* tfull = bars + 2 * S;        // each CTA: accumulator b is ready
+  uint64_t* tempty = tfull + 2;          // leader: both CTAs have drained accumulator b
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  volatile uint32_t* unit_status = tmem_slot + 2;   // two slots, indexed by unit parity
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int64_t pair = blockIdx.x >> 1;
+  const int64_t cta = blockIdx.x;
+  const Plan& plan = args.plan;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * (kPairEpilogueThreads / 32));
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    unit_status[0] = 0;
+    unit_status[1] = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    if constexpr (kMx) {
+      prefetch_tensormap(&tmSfa);
+      prefetch_tensormap(&tmSfb);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, Cf::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // both CTAs' barriers exist before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint32_t full_leader0 = cluster_addr(&full[0], 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      Cursor cur(plan, pair);
+      Unit u;
+      while (ok && cur.next(plan, u)) {
+        int32_t tm, tn;
+        tile_coords(plan, u.tile, tm, tn);
+        const int32_t row0 = tm * 256 + static_cast<int32_t>(rank) * 128;
+        const int32_t col0 = tn * kBN + static_cast<int32_t>(rank) * Cf::kHalfN;
+        for (int32_t k = u.k0; k < u.k1; ++k) {
+          if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, args, kSiteProducer)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Cf::kStageBytes);
+          const uint32_t fb = full_leader0 + stage * 8;
+          uint8_t* sa = ring_a + stage * Cf::kStageA;
+          uint8_t* sb = ring_b + stage * Cf::kStageB;
+          if constexpr (kMx) {
+            tma_load_2d_pair(sa, &tmA, fb, k * 128, row0);
+            tma_load_2d_pair(sb, &tmB, fb, k * 128, col0);
+            // scale blocks: rows of 1 KB = (row block, k-iteration); A: this CTA's 128 rows,
+            // B: both 128-column blocks of the pair's tile.
+            tma_load_2d_pair(ring_sfa + stage * Cf::kStageSfa, &tmSfa, fb, 0,
+                             (tm * 2 + static_cast<int32_t>(rank)) * plan.iters + k);
+            tma_load_2d_pair(ring_sfb + stage * Cf::kStageSfb, &tmSfb, fb, 0,
+                             (tn * 2) * plan.iters + k);
+            tma_load_2d_pair(ring_sfb + stage * Cf::kStageSfb + 1024, &tmSfb, fb, 0,
+                             (tn * 2 + 1) * plan.iters + k);
+          } else {
+            tma_load_2d_pair(sa, &tmA, fb, k * 64, row0);
+            tma_load_2d_pair(sb, &tmB, fb, col0, k * 64);
+            tma_load_2d_pair(sb + 8192, &tmB, fb, col0 + 64, k * 64);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        const int64_t outstanding = issued < S ? issued : S;
+        for (int64_t i = 1; i <= outstanding; ++i) {
+          const int s = static_cast<int>((stage - i + S) % S);
+          const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+          if (!wait_bar_drain(&full[s], par, 100000000ull)) record_error(args, kSiteDrain, -1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (leader)
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      Cursor cur(plan, pair);
+      Unit u;
+      while (ok && cur.next(plan, u)) {
+        if (!wait_bar(&tempty[acc], acc_phase ^ 1u, abort_flag, args, kSiteMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * Cf::kAccCols;
+        for (int32_t k = u.k0; k < u.k1; ++k) {
+          if (!wait_bar(&full[stage], phase, abort_flag, args, kSiteMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(ring_a + stage * Cf::kStageA);
+          const uint32_t b0 = smem_addr(ring_b + stage * Cf::kStageB);
+          if constexpr (kMx) {
+            const uint32_t sf_base = tmem_base + Cf::kAccBufs * Cf::kAccCols;
+            const uint32_t sfa_t = sf_base + stage * Cf::kSfaCols;
+            const uint32_t sfb_t = sf_base + S * Cf::kSfaCols + stage * Cf::kSfbCols;
+            const uint32_t sfa_s = smem_addr(ring_sfa + stage * Cf::kStageSfa);
+            const uint32_t sfb_s = smem_addr(ring_sfb + stage * Cf::kStageSfb);
+#pragma unroll
+            for (int g = 0; g < 2; ++g)
+              tmem_copy_32x128b_x4_pair(sfa_t + g * 4,
+                                        smem_desc(sfa_s + g * 512, 0, 128, kLayoutSwizzleNone));
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int g = 0; g < 2; ++g)
+                tmem_copy_32x128b_x4_pair(
+                    sfb_t + g * 8 + j * 4,
+                    smem_desc(sfb_s + j * 1024 + g * 512, 0, 128, kLayoutSwizzleNone));
+#pragma unroll
+            for (int j = 0; j < Cf::kMmasPerStage; ++j) {
+              const uint32_t g = j >> 1;
+              const uint32_t sf_id = (j & 1) * 2;
+              const uint32_t idesc = Cf::kIdesc | (sf_id << 29) | (sf_id << 4);
+              const uint64_t ad = smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
+              const uint64_t bd = smem_desc(b0 + j * 32, 16, 1024, kLayoutSwizzle128B);
+              mma_mxf4_pair(d_tmem, ad, bd, idesc, sfa_t + g * 4, sfb_t + g * 8,
+                            (k > u.k0 || j > 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < Cf::kMmasPerStage; ++j) {
+              const uint64_t ad = smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
+              const uint64_t bd = smem_desc(b0 + j * 2048, 8192, 1024, kLayoutSwizzle128B);
+              mma_f16_pair(d_tmem, ad, bd, Cf::kIdesc, (k > u.k0 || j > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit_pair(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(&tfull[acc]);
+        if (++acc == Cf::kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      mma_commit_pair_local(mma_done);
+      if (!wait_bar_drain(mma_done, 0, 100000000ull)) record_error(args, kSiteDrain, -1);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;            // which 128 accumulator columns
+    const int row = quarter * 32 + lane;         // tile row within this CTA's 128
+    const int et = threadIdx.x - 64;             // 0..255
+    const uint32_t tempty_leader0 = cluster_addr(&tempty[0], 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int parity = 0;
+    Cursor cur(plan, pair);
+    Unit u;
+    while (cur.next(plan, u)) {
+      int n_contrib = 0;
+      if (u.role == kRoleOwner) {
+        int64_t covered = u.k1;
+        for (int64_t c = pair + 1; covered < plan.iters; ++c, ++n_contrib) {
+          const int64_t len = sk_range_len(plan, c);
+          covered += (len < plan.iters - covered) ? len : (plan.iters - covered);
+        }
+      }
+      if (et == 0) {
+        uint32_t status = kUnitStore;
+        if (!wait_bar(&tfull[acc], acc_phase, abort_flag, args, kSiteEpilogue)) {
+          status = kUnitAbort;
+        } else if (u.role == kRoleOwner) {
+          for (int c = 0; c < n_contrib; ++c) {
+            uint32_t* f = args.flags + 2 * (pair + 1 + c) + rank;
+            if (!wait_flag(f, args.epoch, args.timeout_ns)) {
+              record_error(args, kSiteFlag, u.tile);
+              status = kUnitSkip;
+              break;
+            }
+            *reinterpret_cast<volatile uint32_t*>(f) = 0u;
+          }
+        }
+        unit_status[parity] = status;
+      }
+      named_barrier_sync(1, kPairEpilogueThreads);
+      const uint32_t status = unit_status[parity];
+      if (status == kUnitAbort) break;
+      tc_fence_after();
+
+      // Drain this thread's 128 columns, then hand the accumulator back.
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc) * Cf::kAccCols + half * 128;
+      float v[128];
+      __syncwarp();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t r[32];
+        tmem_load_32cols(t_row + ch * 32, r);
+        tmem_load_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[ch * 32 + j] = __uint_as_float(r[j]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) remote_arrive(tempty_leader0 + acc * 8);
+
+      int32_t tm, tn;
+      tile_coords(plan, u.tile, tm, tn);
+      const int64_t m = static_cast<int64_t>(tm) * 256 + rank * 128 + row;
+      const int64_t n_half = static_cast<int64_t>(tn) * kBN + half * 128;
+      if (u.role == kRoleContrib) {
+        float4* dst = reinterpret_cast<float4*>(args.P + cta * (kBM * kBN)) +
+                      static_cast<int64_t>(half * 4) * 8 * kBM + row;
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          __stcg(dst + q * kBM, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+        __threadfence();
+        named_barrier_sync(1, kPairEpilogueThreads);
+        if (et == 0 && !(args.inject_drop && cta == args.drop_cta))
+          flag_release(args.flags + cta, args.epoch);
+      } else if (status == kUnitStore) {
+        for (int c = 0; c < n_contrib; ++c) {
+          const float4* src =
+              reinterpret_cast<const float4*>(args.P + (2 * (pair + 1 + c) + rank) * (kBM * kBN)) +
+              static_cast<int64_t>(half * 4) * 8 * kBM + row;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            float4 p[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) p[q] = __ldcg(src + (ch * 8 + q) * kBM);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              v[ch * 32 + 4 * q] += p[q].x;
+              v[ch * 32 + 4 * q + 1] += p[q].y;
+              v[ch * 32 + 4 * q + 2] += p[q].z;
+              v[ch * 32 + 4 * q + 3] += p[q].w;
+            }
+            asm volatile("" ::: "memory");   // keep the chunks' loads apart (register pressure)
+          }
+        }
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+          store_row_chunk(args, m, n_half + ch * 32, *reinterpret_cast<float(*)[32]>(&v[ch * 32]));
+      }
+      parity ^= 1;
+      if (++acc == Cf::kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // no CTA leaves while its peer may still signal its barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cf::kTmemCols);
+  }
+}
+
+}  // namespace sk

@@ -108,12 +108,51 @@ def test_plan_fields_follow_the_schedule_rules(lib):
     p = sk.sk_plan(0, 256, 256, 512, 3, "streamk", 148)
     assert (p.tile_n, p.tiles, p.iters, p.grid) == (128, 4, 8, 3)
     assert (p.sk_base, p.sk_extra, p.whole_tiles) == (10, 2, 0)
-    p = sk.sk_plan(0, 1920, 1920, 16384, 0, "hybrid", 148)
+    p = sk.sk_plan(0, 1920, 1920, 16384, 0, "hybrid", 148, {"tile_m": 128})
     assert p.tiles == 225 and p.sk_tiles == 225 % 148 and p.whole_tiles == 148
-    p = sk.sk_plan(1, 8192, 8192, 8192, 0, "streamk", 148)
+    p = sk.sk_plan(1, 8192, 8192, 8192, 0, "streamk", 148, {"tile_m": 128})
     assert (p.tile_n, p.tile_k, p.iters) == (128, 256, 32)
     with pytest.raises(sk.SkError):
         sk.sk_plan(0, 0, 8, 8, 0, "dp", 148)
+
+
+def test_pair_plans():
+    # large problems go to SM pairs: 256 x 256 tiles, grid counted in pairs
+    p = sk.sk_plan(0, 8192, 8192, 8192, 0, "streamk", 152)
+    assert (p.tile_m, p.tile_n, p.ctas_per_tile, p.grid, p.tiles) == (256, 256, 2, 76, 1024)
+    p = sk.sk_plan(1, 8192, 8192, 8192, 0, "persistent", 152)
+    assert (p.tile_m, p.tile_n, p.tile_k, p.iters, p.grid) == (256, 256, 256, 32, 76)
+    # num_sms counts SMs: an odd request leaves one SM unused
+    p = sk.sk_plan(0, 4096, 4096, 4096, 33, "persistent", 152)
+    assert p.ctas_per_tile == 2 and p.grid == 16
+    p = sk.sk_plan(0, 4096, 4096, 4096, 0, "dp", 152)
+    assert p.grid == 256 and p.ctas_per_tile == 2
+    # too few SMs, rows or tiles for a pair: one CTA per tile
+    assert sk.sk_plan(0, 4096, 4096, 4096, 1, "persistent", 152).ctas_per_tile == 1
+    assert sk.sk_plan(0, 4096, 4096, 4096, 3, "streamk", 152).ctas_per_tile == 1
+    assert sk.sk_plan(0, 64, 14336, 4096, 0, "streamk", 152).ctas_per_tile == 1
+    assert sk.sk_plan(0, 256, 256, 512, 0, "streamk", 152).ctas_per_tile == 1
+    # forced choices
+    assert sk.sk_plan(0, 256, 256, 512, 0, "dp", 152, {"tile_m": 256}).ctas_per_tile == 2
+    assert sk.sk_plan(0, 8192, 8192, 8192, 0, "dp", 152, {"tile_n": 128}).ctas_per_tile == 1
+    for bad in [{"tile_m": 256, "tile_n": 128}, {"tile_m": 64}]:
+        with pytest.raises(sk.SkError):
+            sk.sk_plan(0, 1024, 1024, 1024, 0, "dp", 152, bad)
+    with pytest.raises(sk.SkError):
+        sk.sk_plan(0, 1024, 1024, 1024, 1, "dp", 152, {"tile_m": 256})
+
+
+@pytest.mark.parametrize("mode", ["dp", "persistent", "streamk", "hybrid"])
+@pytest.mark.parametrize("shape", [(8192, 8192, 8192), (1920, 1920, 16384), (300, 264, 200),
+                                   (1000, 3000, 640)])
+@pytest.mark.parametrize("g", [2, 7, 33, 0])
+def test_pair_scheduler_matches_oracle_restatement(mode, shape, g):
+    M, N, K = shape
+    plan = sk.sk_plan(0, M, N, K, g, mode, 152, {"tile_m": 256})
+    assert plan.ctas_per_tile == 2
+    got = sk.sk_plan_segments(plan)
+    want = oracle.schedule(sk.MODES[mode], plan.tiles, plan.iters, plan.grid)
+    assert np.array_equal(got[:, :5], want)
 
 
 def _same_split(mode, M, N, K, g_req, sms, tile_n):
@@ -138,8 +177,14 @@ def test_kernel_scheduler_matches_oracle_restatement(lib, mode, shape, g):
                                            (1000, 3000, 640, 5, 37), (128, 256, 64, 1, 3),
                                            (640, 128, 4096, 3, 7), (256, 256, 512, 16, 3),
                                            (2048, 512, 128, 4, 148)])
-def test_raster_is_a_bijection_onto_the_tile_grid(lib, mode, M, N, K, group, g):
-    plan = sk.sk_plan(0, M, N, K, g, mode, 152, {"tile_n": 128, "raster_group": group})
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_raster_is_a_bijection_onto_the_tile_grid(lib, mode, M, N, K, group, g, tile_m):
+    if tile_m == 256 and g < 2:
+        pytest.skip("pairs need two SMs")
+    opts = {"raster_group": group, "tile_m": tile_m}
+    if tile_m == 128:
+        opts["tile_n"] = 128
+    plan = sk.sk_plan(0, M, N, K, g, mode, 152, opts)
     segs = sk.sk_plan_segments(plan)
     owned = segs[segs[:, 2] == 0]          # the piece holding k = 0 of each tile
     cells = list(map(tuple, owned[:, 5:7].tolist()))

@@ -42,16 +42,20 @@ def test_addmm_256_streamk_over_3_ctas_splits_two_tiles():
 
 # ---- exact integer inputs: bit-exact in every schedule --------------------------------------
 
+TILES = {"128x128": {"tile_m": 128, "tile_n": 128}, "128x256": {"tile_m": 128, "tile_n": 256},
+         "pair256": {"tile_m": 256}}
+
+
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("shape", [(200, 136, 200), (1, 8, 8), (128, 128, 64), (129, 264, 72),
-                                   (384, 1024, 512), (640, 256, 8)])
-@pytest.mark.parametrize("tile_n", [128, 256])
+                                   (384, 1024, 512), (640, 256, 8), (520, 776, 1000)])
+@pytest.mark.parametrize("tile", list(TILES))
 @pytest.mark.parametrize("out", ["bf16", "f32"])
-def test_integer_inputs_are_bit_exact(mode, shape, tile_n, out):
+def test_integer_inputs_are_bit_exact(mode, shape, tile, out):
     M, N, K = shape
     p = inputs.bf16_problem(M, N, K, seed=M + 7 * N + 13 * K, integer=True,
                             bias="bf16_int" if out == "bf16" else "f32_int")
-    c = gu.run_bf16(p, out=out, mode=mode, num_sms=5, options={"tile_n": tile_n})
+    c = gu.run_bf16(p, out=out, mode=mode, num_sms=10, options=TILES[tile])
     want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]),
                                oracle.BF16 if out == "bf16" else oracle.F32)
     want_bits = want if out == "bf16" else want.view(np.uint32)
@@ -60,9 +64,13 @@ def test_integer_inputs_are_bit_exact(mode, shape, tile_n, out):
 
 @pytest.mark.parametrize("mode", ["persistent", "streamk", "hybrid"])
 @pytest.mark.parametrize("num_sms", [1, 2, 3, 7, 16, 64, 151, 152, 0, 1000])
-def test_num_sms_sweep_integer_bit_exact(mode, num_sms):
-    p = inputs.bf16_problem(520, 776, 1000, seed=77, integer=True, bias="bf16_int")
-    c = gu.run_bf16(p, out="bf16", mode=mode, num_sms=num_sms)
+@pytest.mark.parametrize("tile", ["auto", "pair256"])
+def test_num_sms_sweep_integer_bit_exact(mode, num_sms, tile):
+    if tile == "pair256" and 0 < num_sms < 2:
+        pytest.skip("a pair needs two SMs")
+    p = inputs.bf16_problem(1040, 776, 1000, seed=77, integer=True, bias="bf16_int")
+    c = gu.run_bf16(p, out="bf16", mode=mode, num_sms=num_sms,
+                    options=None if tile == "auto" else TILES[tile])
     want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), oracle.BF16)
     assert np.array_equal(gu.host_bits(c), want)
 
@@ -82,10 +90,10 @@ def test_no_bias_and_zero_a_give_bias_rows():
 # ---- random inputs --------------------------------------------------------------------------
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("tile_n", [128, 256])
-def test_random_inputs_match_oracle(mode, tile_n):
+@pytest.mark.parametrize("tile", list(TILES))
+def test_random_inputs_match_oracle(mode, tile):
     p = inputs.bf16_problem(640, 896, 1544, seed=5, operand_scale="sqrt_k", bias="bf16_uniform")
-    c = gu.run_bf16(p, out="bf16", mode=mode, num_sms=0, options={"tile_n": tile_n})
+    c = gu.run_bf16(p, out="bf16", mode=mode, num_sms=0, options=TILES[tile])
     ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "bf16")
     gu.assert_close(gu.host_values(c), ref, "bf16", mode)
 
@@ -165,6 +173,34 @@ def test_capture_without_reserved_workspace_is_refused():
         st = sk.sk_gemm_bf16(a.data_ptr(), a.data_ptr(), None, c.data_ptr(), 1, 256, 256, 256,
                              0, 2, s.cuda_stream)
     assert st == sk.SK_ERR_UNSUPPORTED
+
+
+def test_pair_streamk_wait_that_runs_out_reports_timeout():
+    # 2048 x 256 x 4096 on 4 pairs: pair 1 (CTAs 2, 3) continues the tile pair 0 owns; CTA 3
+    # never publishes, so CTA 1 (the rank-1 half of the owner) times out.
+    p = inputs.bf16_problem(2048, 256, 4096, seed=4, bias="bf16_uniform")
+    a, b, bias = gu.dev_bf16(p["A"]), gu.dev_bf16(p["B"]), gu.dev_bias(p["bias"])
+    plan = sk.sk_plan(0, 2048, 256, 4096, 8, "streamk", 152, {"tile_m": 256})
+    segs = sk.sk_plan_segments(plan)
+    assert plan.ctas_per_tile == 2 and plan.grid == 4
+    assert segs[(segs[:, 0] == 1)][0, 4] == 2          # pair 1 starts with a contribution
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        sk.gemm_bf16(a, b, bias, mode="streamk", num_sms=8, stream=s,
+                     options={"tile_m": 256, "inject_faults": 1, "drop_release_cta": 3,
+                              "spin_timeout_ns": 20_000_000})
+    assert sk.sk_stream_status(s.cuda_stream) == sk.SK_ERR_TIMEOUT
+    c = gu.run_bf16(p, out="bf16", mode="streamk", num_sms=8, stream=s, options={"tile_m": 256})
+    ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "bf16")
+    gu.assert_close(gu.host_values(c), ref, "bf16")
+
+
+def test_device_caps_report_the_pair_capacity():
+    caps = sk.sk_device_caps(0)
+    assert caps["cc"] == (10, 3)
+    assert caps["setup_error"] == [0] * 5
+    assert all(n >= 1 for n in caps["ctas_per_sm"])
+    assert all(2 * n <= caps["sm_count"] and n >= 1 for n in caps["max_pair_clusters"])
 
 
 def test_streamk_wait_that_runs_out_reports_timeout():

@@ -17,18 +17,22 @@ def _device(cuda_device):
     yield
 
 
+TILES = {"128x128": {"tile_m": 128}, "pair256": {"tile_m": 256}}
+
+
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("shape", [(128, 128, 256), (200, 136, 288), (300, 77, 96), (1, 1, 32),
-                                   (257, 383, 1056), (64, 1000, 512)])
+                                   (257, 383, 1056), (64, 1000, 512), (640, 520, 800)])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
-def test_small_scale_range_is_bit_exact(mode, shape, out):
+@pytest.mark.parametrize("tile", list(TILES))
+def test_small_scale_range_is_bit_exact(mode, shape, out, tile):
     # scale exponents in [-1, 1]: every partial sum is exact in fp32 at these K, so the only
     # rounding is the final one (an fp32 bias is added in that same single rounding; a bf16
     # output gets no bias here, since fp32 add then bf16 cast would round twice)
     M, N, K = shape
     p = inputs.mxfp4_problem(M, N, K, seed=M * 3 + N * 5 + K, exp_range=1,
                              bias="none" if out == "bf16" else "f32_normal")
-    c = gu.run_mxfp4(p, out=out, mode=mode, num_sms=6)
+    c = gu.run_mxfp4(p, out=out, mode=mode, num_sms=12, options=TILES[tile])
     want = oracle.round_output(
         oracle.addmm_mxfp4(p["A"], p["A_scale"], p["B"], p["B_scale"], p["bias"]),
         oracle.BF16 if out == "bf16" else oracle.F32)
@@ -37,20 +41,23 @@ def test_small_scale_range_is_bit_exact(mode, shape, out):
 
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("num_sms", [1, 3, 17, 0])
-def test_full_scale_range_matches_oracle(mode, num_sms):
-    p = inputs.mxfp4_problem(384, 520, 2048, seed=41, exp_range=4, bias="bf16_uniform")
-    c = gu.run_mxfp4(p, out="bf16", mode=mode, num_sms=num_sms)
+@pytest.mark.parametrize("tile", ["auto", "128x128"])
+def test_full_scale_range_matches_oracle(mode, num_sms, tile):
+    p = inputs.mxfp4_problem(768, 520, 2048, seed=41, exp_range=4, bias="bf16_uniform")
+    c = gu.run_mxfp4(p, out="bf16", mode=mode, num_sms=num_sms,
+                     options=None if tile == "auto" else TILES[tile])
     ref = gu.reference(oracle.addmm_mxfp4(p["A"], p["A_scale"], p["B"], p["B_scale"], p["bias"]),
                        "bf16")
     gu.assert_close(gu.host_values(c), ref, "bf16", f"{mode}/{num_sms}")
 
 
-def test_nan_scale_propagates_to_its_column_only():
-    p = inputs.mxfp4_problem(256, 256, 256, seed=9, exp_range=2)
-    p["B_scale"][17, 3] = 255
-    c = gu.host_values(gu.run_mxfp4(p, out="f32", mode="streamk", num_sms=5))
-    assert np.all(np.isnan(c[:, 17]))
-    assert not np.isnan(np.delete(c, 17, axis=1)).any()
+@pytest.mark.parametrize("tile", list(TILES))
+def test_nan_scale_propagates_to_its_column_only(tile):
+    p = inputs.mxfp4_problem(512, 512, 512, seed=9, exp_range=2)
+    p["B_scale"][300, 3] = 255
+    c = gu.host_values(gu.run_mxfp4(p, out="f32", mode="streamk", num_sms=6, options=TILES[tile]))
+    assert np.all(np.isnan(c[:, 300]))
+    assert not np.isnan(np.delete(c, 300, axis=1)).any()
 
 
 def test_mxfp4_equals_bf16_path_on_decoded_operands():
