@@ -193,11 +193,12 @@ def tile_efficiency(plan, sm_count):
     per_cta = np.zeros(plan.grid, dtype=np.int64)
     np.add.at(per_cta, segs[:, 0], segs[:, 3] - segs[:, 2])
     total = int(per_cta.sum())
-    if plan.grid > sm_count:   # data-parallel: CTAs run in waves of one per SM
-        per_sm = np.zeros(sm_count, dtype=np.int64)
-        np.add.at(per_sm, np.arange(plan.grid) % sm_count, per_cta)
-        return total / (sm_count * int(per_sm.max()))
-    return total / (plan.grid * int(per_cta.max()))
+    slots = sm_count // plan.ctas_per_tile   # workers that run at once: SMs, or SM pairs
+    if plan.grid > slots:      # data-parallel: workers run in waves of one per slot
+        per_slot = np.zeros(slots, dtype=np.int64)
+        np.add.at(per_slot, np.arange(plan.grid) % slots, per_cta)
+        return total / (slots * int(per_slot.max()))
+    return total / (slots * int(per_cta.max()))
 
 
 # ---------------------------------------------------------------------------------------
@@ -242,19 +243,29 @@ class Problem:
     def d2h_bytes(self):
         return self.C.numel() * self.C.element_size()
 
-    def call(self, mode, num_sms, stream_ptr, dev=None):
-        """One addmm through the C ABI.  Returns the status code."""
+    def call(self, mode, num_sms, stream_ptr, dev=None, options=None):
+        """One addmm through the C ABI (the _ex form when options are given).  Returns the
+        status code."""
         import sm_constrained_persistent_gb300 as sk
         d = self.dev if dev is None else dev
         bias = d["bias"].data_ptr() if "bias" in d else None
         od = sk.SK_BF16 if self.out_dtype.itemsize == 2 else sk.SK_F32
         m = sk.MODES[mode]
         if self.fmt == "bf16":
-            return sk.sk_gemm_bf16(d["A"].data_ptr(), d["B"].data_ptr(), bias, self.C.data_ptr(),
-                                   od, self.M, self.N, self.K, num_sms, m, stream_ptr)
-        return sk.sk_gemm_mxfp4(d["A"].data_ptr(), d["A_scale"].data_ptr(), d["B"].data_ptr(),
-                                d["B_scale"].data_ptr(), bias, self.C.data_ptr(), od, self.M,
-                                self.N, self.K, num_sms, m, stream_ptr)
+            if options is None:
+                return sk.sk_gemm_bf16(d["A"].data_ptr(), d["B"].data_ptr(), bias,
+                                       self.C.data_ptr(), od, self.M, self.N, self.K, num_sms, m,
+                                       stream_ptr)
+            return sk.sk_gemm_bf16_ex(d["A"].data_ptr(), d["B"].data_ptr(), bias,
+                                      self.C.data_ptr(), od, self.M, self.N, self.K, num_sms, m,
+                                      options, stream_ptr)
+        if options is None:
+            return sk.sk_gemm_mxfp4(d["A"].data_ptr(), d["A_scale"].data_ptr(), d["B"].data_ptr(),
+                                    d["B_scale"].data_ptr(), bias, self.C.data_ptr(), od, self.M,
+                                    self.N, self.K, num_sms, m, stream_ptr)
+        return sk.sk_gemm_mxfp4_ex(d["A"].data_ptr(), d["A_scale"].data_ptr(), d["B"].data_ptr(),
+                                   d["B_scale"].data_ptr(), bias, self.C.data_ptr(), od, self.M,
+                                   self.N, self.K, num_sms, m, options, stream_ptr)
 
     def kernels_per_call(self):
         return 1 if self.fmt == "bf16" else 3   # MXFP4: two scale-layout kernels + the GEMM
@@ -269,7 +280,7 @@ def needs_flush(prob):
     return operand_bytes < L2_FLUSH_BYTES
 
 
-def time_calls(prob, mode, num_sms, steps, warmup, dist=None):
+def time_calls(prob, mode, num_sms, steps, warmup, dist=None, options=None):
     """Device time of `steps` calls (after `warmup`), CUDA events on the launch stream,
     barrier + synchronize on both sides.  Back to back when the operands exceed L2; otherwise
     a 256 MiB write flushes L2 before each call and only the calls are timed.
@@ -281,7 +292,7 @@ def time_calls(prob, mode, num_sms, steps, warmup, dist=None):
     flush = needs_flush(prob)
     scrub = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=prob.device) if flush else None
     for _ in range(warmup):
-        st = prob.call(mode, num_sms, sp)
+        st = prob.call(mode, num_sms, sp, options=options)
         if st != 0:
             raise RuntimeError(f"warm-up call failed: {sk.STATUS.get(st, st)}")
     torch.cuda.synchronize()
@@ -295,7 +306,7 @@ def time_calls(prob, mode, num_sms, steps, warmup, dist=None):
         if flush:
             scrub.fill_(1.0)
         s.record(stream)
-        prob.call(mode, num_sms, sp)
+        prob.call(mode, num_sms, sp, options=options)
         e.record(stream)
     torch.cuda.synchronize()
     barrier(dist)
@@ -436,37 +447,71 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def extras(prob, sm_count, dist):
-    """Per-schedule throughput of the benchmark workloads (each timed on its own after the
-    headline region: 3 warm-up + 10 timed calls)."""
-    import torch
+def _time_modes(pr, modes, sm_count, peak, dist, num_sms=0, options=None, steps=10, warmup=3):
+    """ms, TFLOPS, % of peak, grid, tile and tile-quantisation efficiency per mode."""
     import sm_constrained_persistent_gb300 as sk
+    res = {}
+    for mode in modes:
+        total, _ = time_calls(pr, mode, num_sms, steps, warmup, dist, options)
+        ms = total / steps
+        plan = sk.sk_plan(0 if pr.fmt == "bf16" else 1, pr.M, pr.N, pr.K, num_sms, mode, sm_count,
+                          options)
+        tflops = pr.flops / (ms * 1e-3) / 1e12
+        res[mode] = {"ms": round(ms, 4), "tflops": round(tflops, 1),
+                     "pct_peak": round(100 * tflops / peak, 1), "grid": plan.grid,
+                     "ctas": plan.grid * plan.ctas_per_tile,
+                     "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}",
+                     "tile_quant_eff": round(tile_efficiency(plan, sm_count), 4)}
+    return res
+
+
+def extras(prob, sm_count, dist):
+    """Per-schedule throughput of the benchmark workloads, each timed on its own after the
+    headline region (3 warm-up + 10 timed calls per entry), and the SM-constrained sweep."""
+    import torch
     out = {}
     peaks, _ = measured_peaks()
     bpeak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    jobs = [(prob.name, prob, ["dp", "persistent", "streamk", "hybrid"])]
-    for name, modes in [("gemm_bf16_1920x1920x16384", ["dp", "persistent", "streamk", "hybrid"]),
-                        ("addmm_mxfp4_8192", ["dp", "persistent", "streamk", "hybrid"])]:
-        if name != prob.name:
-            jobs.append((name, None, modes))
-    for name, pr, modes in jobs:
-        if pr is None:
-            pr = Problem(name, prob.device)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    modes = ["dp", "persistent", "streamk", "hybrid"]
+    cache = {prob.name: prob}
+
+    def get(name):
+        if name not in cache:
+            cache[name] = Problem(name, prob.device)
+        return cache[name]
+
+    for name in ["addmm_bf16_8192", "addmm_mxfp4_8192"]:
+        pr = get(name)
         peak = bpeak if pr.fmt == "bf16" else bpeak * FP4_OVER_BF16
-        res = {}
-        for mode in modes:
-            total, per = time_calls(pr, mode, 0, 10, 3, dist)
-            ms = total / 10
-            plan = sk.sk_plan(0 if pr.fmt == "bf16" else 1, pr.M, pr.N, pr.K, 0, mode, sm_count)
-            tflops = pr.flops / (ms * 1e-3) / 1e12
-            res[mode] = {"ms": round(ms, 4), "tflops": round(tflops, 1),
-                         "pct_peak": round(100 * tflops / peak, 1), "grid": plan.grid,
-                         "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}",
-                         "tile_quant_eff": round(tile_efficiency(plan, sm_count), 4)}
-        out[name] = res
-        if pr is not prob:
-            del pr
-            torch.cuda.empty_cache()
+        out[name] = _time_modes(pr, modes, sm_count, peak, dist)
+    # the wave-quantised shape: its stated 128x128 tiles (225 tiles) and the automatic choice
+    pr = get("gemm_bf16_1920x1920x16384")
+    out["gemm_bf16_1920x1920x16384"] = {
+        "tile_128x128": _time_modes(pr, modes, sm_count, bpeak, dist,
+                                    options={"tile_m": 128, "tile_n": 128}),
+        "auto": _time_modes(pr, modes, sm_count, bpeak, dist)}
+    # SM-constrained persistent sweep: time and TFLOPS per num_sms
+    sweep = {}
+    for name in ["gemm_bf16_4096", "gemm_bf16_skinny_64x14336x4096"]:
+        pr = get(name)
+        rows = {}
+        for ns in [1, 16, 32, 64, 128, sm_count]:
+            r = _time_modes(pr, ["persistent"], sm_count, bpeak, dist, num_sms=ns,
+                            steps=5 if ns < 16 else 10, warmup=2)["persistent"]
+            r["tflops_per_sm"] = round(r["tflops"] / ns, 2)
+            if "skinny" in name:
+                bytes_moved = sum(t.numel() * t.element_size() for t in pr.dev.values()) + \
+                    pr.C.numel() * pr.C.element_size()
+                r["gbs"] = round(bytes_moved / (r["ms"] * 1e-3) / 1e9, 1)
+                r["pct_hbm"] = round(100 * r["gbs"] / hbm, 1)
+            rows[str(ns)] = r
+        sweep[name] = rows
+    out["num_sms_sweep_persistent"] = sweep
+    for name in list(cache):
+        if cache[name] is not prob:
+            del cache[name]
+    torch.cuda.empty_cache()
     return out
 
 

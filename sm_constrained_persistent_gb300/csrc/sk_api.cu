@@ -407,10 +407,9 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   if (format == 1) {
     uint8_t* sfa = ws->sf;
     uint8_t* sfb = ws->sf + mx.a_row_blocks * mx.kgroups * 512;
-    if (sk::mx_scale_prep(static_cast<const uint8_t*>(A_scale), M, K / 32, mx.a_row_blocks,
-                          mx.kgroups, sfa, di->sm_count, stream) != cudaSuccess ||
-        sk::mx_scale_prep(static_cast<const uint8_t*>(B_scale), N, K / 32, mx.b_row_blocks,
-                          mx.kgroups, sfb, di->sm_count, stream) != cudaSuccess)
+    if (sk::mx_scale_prep(static_cast<const uint8_t*>(A_scale), M, mx.a_row_blocks,
+                          static_cast<const uint8_t*>(B_scale), N, mx.b_row_blocks, K / 32,
+                          mx.kgroups, ws->sf, stream) != cudaSuccess)
       return SK_ERR_CUDA;
     a.sfa = sfa;
     a.sfb = sfb;

@@ -8,41 +8,44 @@ cudaError_t launch_bf16(int tile_n, const Launch& l);
 cudaError_t setup_bf16(int tile_n, int* ctas_per_sm);
 size_t smem_bf16(int tile_n);
 
-__global__ void __launch_bounds__(256) mx_scale_prep_kernel(const uint8_t* __restrict__ scales,
-                                                            int64_t rows, int64_t kblocks,
-                                                            int64_t row_blocks, int64_t kgroups,
-                                                            uint32_t* __restrict__ out) {
-  const int64_t total = row_blocks * kgroups * 128;   // 32-bit words
-  for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < total;
-       w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t within = w % 128;
-    const int64_t group = w / 128;
-    const int64_t g = group % kgroups;
-    const int64_t rb = group / kgroups;
-    const int64_t i = within / 4;
-    const int64_t c = within % 4;
-    const int64_t r = rb * 128 + c * 32 + i;
-    uint32_t word = 0;
+// One 128-thread block per 512-byte output group (row block rb, k group g): thread t writes
+// word t, i.e. scales (row rb*128 + 32*(t%4) + t/4, blocks 4g .. 4g+3).  blockIdx.y < a_blocks
+// covers A, the rest B.
+__global__ void __launch_bounds__(128) mx_scale_prep_kernel(
+    const uint8_t* __restrict__ sa, int32_t a_rows, int32_t a_blocks, const uint8_t* __restrict__ sb,
+    int32_t b_rows, int32_t kblocks, int32_t kgroups, uint32_t* __restrict__ out) {
+  const int32_t g = blockIdx.x;
+  int32_t rb = blockIdx.y;
+  const bool is_a = rb < a_blocks;
+  const uint8_t* s = is_a ? sa : sb;
+  const int32_t rows = is_a ? a_rows : b_rows;
+  const int32_t t = threadIdx.x;
+  const int32_t r = (is_a ? rb : rb - a_blocks) * 128 + (t & 3) * 32 + (t >> 2);
+  const int32_t kb0 = g * 4;
+  uint32_t word;
+  if (r < rows && kb0 + 4 <= kblocks && (kblocks & 3) == 0) {
+    word = __ldg(reinterpret_cast<const uint32_t*>(s + static_cast<int64_t>(r) * kblocks + kb0));
+  } else {
+    word = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int64_t kb = g * 4 + j;
-      const uint32_t byte = (r < rows && kb < kblocks) ? scales[r * kblocks + kb] : 127u;
+      const int32_t kb = kb0 + j;
+      const uint32_t byte =
+          (r < rows && kb < kblocks) ? s[static_cast<int64_t>(r) * kblocks + kb] : 127u;
       word |= byte << (8 * j);
     }
-    out[w] = word;
   }
+  out[(static_cast<int64_t>(rb) * kgroups + g) * 128 + t] = word;
 }
 
-cudaError_t mx_scale_prep(const uint8_t* scales, int64_t rows, int64_t kblocks,
-                          int64_t row_blocks, int64_t kgroups, uint8_t* out, int sm_count,
-                          cudaStream_t stream) {
-  const int64_t total = row_blocks * kgroups * 128;
-  int64_t blocks = (total + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  mx_scale_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      scales, rows, kblocks, row_blocks, kgroups, reinterpret_cast<uint32_t*>(out));
+cudaError_t mx_scale_prep(const uint8_t* a_scales, int64_t a_rows, int64_t a_row_blocks,
+                          const uint8_t* b_scales, int64_t b_rows, int64_t b_row_blocks,
+                          int64_t kblocks, int64_t kgroups, uint8_t* out, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(kgroups), static_cast<unsigned>(a_row_blocks + b_row_blocks));
+  mx_scale_prep_kernel<<<grid, 128, 0, stream>>>(
+      a_scales, static_cast<int32_t>(a_rows), static_cast<int32_t>(a_row_blocks), b_scales,
+      static_cast<int32_t>(b_rows), static_cast<int32_t>(kblocks), static_cast<int32_t>(kgroups),
+      reinterpret_cast<uint32_t*>(out));
   return cudaGetLastError();
 }
 

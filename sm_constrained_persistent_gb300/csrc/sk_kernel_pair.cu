@@ -9,7 +9,7 @@ static cudaError_t launch_pair(const Launch& l) {
   using Cf = PairCfg<kMx>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(l.grid), 1, 1);
-  cfg.blockDim = dim3(kPairThreads, 1, 1);
+  cfg.blockDim = dim3(pair_threads<kMx>(), 1, 1);
   cfg.dynamicSmemBytes = Cf::kSmemBytes;
   cfg.stream = l.stream;
   cfg.attrs = nullptr;
@@ -27,7 +27,7 @@ static cudaError_t setup_pair(int* max_clusters) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kPairThreads, 1, 1);
+  cfg.blockDim = dim3(pair_threads<kMx>(), 1, 1);
   cfg.dynamicSmemBytes = Cf::kSmemBytes;
   e = cudaOccupancyMaxActiveClusters(max_clusters, gemm_pair_kernel<kMx>, &cfg);
   if (e == cudaSuccess && *max_clusters > 0) return e;

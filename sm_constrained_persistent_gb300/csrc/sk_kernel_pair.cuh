@@ -15,6 +15,10 @@
 //               columns [128*h, 128*h+128), h = (w-2)/4.  Each thread first drains its 128
 //               accumulator columns into registers and releases the accumulator to the
 //               leader, then spills (contribution) or aggregates + bias + casts + stores.
+//   warp 10     (MXFP4 only) in the leader, one lane copies each stage's scale factors from
+//               shared to tensor memory (tcgen05.cp) and commits them to that stage's
+//               "scales ready" barrier, which the MMA thread waits on; keeping the copies off
+//               the MMA thread lets them overlap the previous stage's MMAs.
 // MXFP4 keeps one accumulator (256 columns) so that the per-stage scale-factor slots fit in
 // the 512 tensor-memory columns; the fast drain keeps the MMA's wait for it short.  bf16 keeps
 // two accumulators.
@@ -24,8 +28,10 @@
 
 namespace sk {
 
-constexpr int kPairThreads = 320;
 constexpr int kPairEpilogueThreads = 256;
+// 2 issuing warps + 8 epilogue warps; MXFP4 adds a warp that copies scale factors to TMEM.
+template <bool kMx>
+constexpr int pair_threads() { return kMx ? 352 : 320; }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -141,7 +147,8 @@ struct PairCfg {
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kAccBufs * kAccCols + (kMx ? kStages * (kSfaCols + kSfbCols) : 0) <= kTmemCols,
                 "tensor memory budget");
-  static constexpr int kBarrierBytes = 256;
+  static constexpr int kBarrierBytes = 512;
+  static_assert((3 * kStages + 6) * 8 + 16 <= kBarrierBytes, "barrier area");
   static constexpr size_t kSmemBytes =
       1024 + static_cast<size_t>(kStages) * kStageBytes + kBarrierBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -152,10 +159,10 @@ struct PairCfg {
              (uint32_t(256 >> 4) << 24));
 };
 
-// Registers are granted per 128-thread warpgroup, so 320 threads are charged as 384: the
-// launch bound caps the kernel at 65536 / 384 -> 168 registers per thread.
+// Registers are granted per 128-thread warpgroup, so 320 or 352 threads are charged as 384:
+// the launch bound caps the kernel at 65536 / 384 -> 168 registers per thread.
 template <bool kMx>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSfa,
                      const __grid_constant__ CUtensorMap tmSfb, const __grid_constant__ Args args) {
@@ -175,7 +182,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   uint64_t* tfull = bars + 2 * S;        // each CTA: accumulator b is ready
   uint64_t* tempty = tfull + 2;          // leader: both CTAs have drained accumulator b
   uint64_t* mma_done = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* sf_ready = mma_done + 1;     // leader, MXFP4: stage's scales are in TMEM
+  uint64_t* cp_done = sf_ready + S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cp_done + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* unit_status = tmem_slot + 2;   // two slots, indexed by unit parity
 
@@ -197,6 +206,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       mbar_init(&tempty[b], 2 * (kPairEpilogueThreads / 32));
     }
     mbar_init(mma_done, 1);
+    for (int st = 0; st < S; ++st) mbar_init(&sf_ready[st], 1);
+    mbar_init(cp_done, 1);
     *abort_flag = 0;
     unit_status[0] = 0;
     unit_status[1] = 0;
@@ -292,7 +303,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * Cf::kAccCols;
         for (int32_t k = u.k0; k < u.k1; ++k) {
-          if (!wait_bar(&full[stage], phase, abort_flag, args, kSiteMma)) {
+          // MXFP4: the scales-ready barrier also implies the stage's data has landed.
+          if (!wait_bar(kMx ? &sf_ready[stage] : &full[stage], phase, abort_flag, args,
+                        kSiteMma)) {
             ok = false;
             break;
           }
@@ -303,19 +316,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             const uint32_t sf_base = tmem_base + Cf::kAccBufs * Cf::kAccCols;
             const uint32_t sfa_t = sf_base + stage * Cf::kSfaCols;
             const uint32_t sfb_t = sf_base + S * Cf::kSfaCols + stage * Cf::kSfbCols;
-            const uint32_t sfa_s = smem_addr(ring_sfa + stage * Cf::kStageSfa);
-            const uint32_t sfb_s = smem_addr(ring_sfb + stage * Cf::kStageSfb);
-#pragma unroll
-            for (int g = 0; g < 2; ++g)
-              tmem_copy_32x128b_x4_pair(sfa_t + g * 4,
-                                        smem_desc(sfa_s + g * 512, 0, 128, kLayoutSwizzleNone));
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-              for (int g = 0; g < 2; ++g)
-                tmem_copy_32x128b_x4_pair(
-                    sfb_t + g * 8 + j * 4,
-                    smem_desc(sfb_s + j * 1024 + g * 512, 0, 128, kLayoutSwizzleNone));
 #pragma unroll
             for (int j = 0; j < Cf::kMmasPerStage; ++j) {
               const uint32_t g = j >> 1;
@@ -349,6 +349,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       }
       mma_commit_pair_local(mma_done);
       if (!wait_bar_drain(mma_done, 0, 100000000ull)) record_error(args, kSiteDrain, -1);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------------ scale copies (MXFP4)
+    if constexpr (kMx) {
+      if (leader && lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        Cursor cur(plan, pair);
+        Unit u;
+        while (ok && cur.next(plan, u)) {
+          for (int32_t k = u.k0; k < u.k1; ++k) {
+            if (!wait_bar(&full[stage], phase, abort_flag, args, kSiteMma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sf_base = tmem_base + Cf::kAccBufs * Cf::kAccCols;
+            const uint32_t sfa_t = sf_base + stage * Cf::kSfaCols;
+            const uint32_t sfb_t = sf_base + S * Cf::kSfaCols + stage * Cf::kSfbCols;
+            const uint32_t sfa_s = smem_addr(ring_sfa + stage * Cf::kStageSfa);
+            const uint32_t sfb_s = smem_addr(ring_sfb + stage * Cf::kStageSfb);
+#pragma unroll
+            for (int g = 0; g < 2; ++g)
+              tmem_copy_32x128b_x4_pair(sfa_t + g * 4,
+                                        smem_desc(sfa_s + g * 512, 0, 128, kLayoutSwizzleNone));
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int g = 0; g < 2; ++g)
+                tmem_copy_32x128b_x4_pair(
+                    sfb_t + g * 8 + j * 4,
+                    smem_desc(sfb_s + j * 1024 + g * 512, 0, 128, kLayoutSwizzleNone));
+            mma_commit_pair_local(&sf_ready[stage]);
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        mma_commit_pair_local(cp_done);
+        if (!wait_bar_drain(cp_done, 0, 100000000ull)) record_error(args, kSiteDrain, -1);
+      }
     }
   } else {
     // ------------------------------------------------------------------ epilogue
@@ -398,14 +441,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                              static_cast<uint32_t>(acc) * Cf::kAccCols + half * 128;
       float v[128];
       __syncwarp();
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t r[32];
-        tmem_load_32cols(t_row + ch * 32, r);
-        tmem_load_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[ch * 32 + j] = __uint_as_float(r[j]);
-      }
+      tmem_load_64cols(t_row, reinterpret_cast<uint32_t*>(v));
+      tmem_load_64cols(t_row + 64, reinterpret_cast<uint32_t*>(v) + 64);
+      tmem_load_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) remote_arrive(tempty_leader0 + acc * 8);

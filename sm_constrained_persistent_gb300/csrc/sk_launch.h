@@ -44,11 +44,12 @@ cudaError_t pair_variant_setup(int variant, int* max_clusters);
 cudaError_t pair_variant_launch(int variant, const Launch& l);
 size_t pair_variant_smem_bytes(int variant);
 
-// Rearranges row-major [rows][kblocks] E8M0 scales into [row_blocks][kgroups][512]: in group
-// (rb, g), byte 16*i + 4*c + j holds scale (row rb*128 + 32*c + i, block 4*g + j); positions
-// outside the matrix hold 127 (scale 1.0, so the zero-filled operand padding stays 0).
-cudaError_t mx_scale_prep(const uint8_t* scales, int64_t rows, int64_t kblocks,
-                          int64_t row_blocks, int64_t kgroups, uint8_t* out, int sm_count,
-                          cudaStream_t stream);
+// Rearranges the row-major [rows][kblocks] E8M0 scales of A and of B into one buffer of
+// [row_blocks][kgroups][512]: A's row blocks first, then B's.  In group (rb, g), byte
+// 16*i + 4*c + j holds scale (row rb*128 + 32*c + i, block 4*g + j); positions outside the
+// matrix hold 127 (scale 1.0, so the zero-filled operand padding stays 0).  One launch.
+cudaError_t mx_scale_prep(const uint8_t* a_scales, int64_t a_rows, int64_t a_row_blocks,
+                          const uint8_t* b_scales, int64_t b_rows, int64_t b_row_blocks,
+                          int64_t kblocks, int64_t kgroups, uint8_t* out, cudaStream_t stream);
 
 }  // namespace sk
