@@ -150,10 +150,13 @@ struct Segment {
 //  * Stream-K: the tiles x k-iterations of the Stream-K region, taken in linear order
 //    (tile-major, then k), are split into g contiguous ranges whose lengths differ by at
 //    most one (the first (total mod g) ranges are one longer).  A range piece that holds
-//    k = 0 of its tile makes that CTA the tile's owner; a piece that starts past k = 0 is
-//    a partial contribution that the owner adds in before the bias.
+//    k = 0 of its tile makes that CTA the tile's owner; a piece that starts past k = 0 is a
+//    partial contribution that the owner adds in before the bias.
 //  * hybrid: the last (tiles mod g) tiles form the Stream-K region, the others are run
-//    whole, round-robin; every CTA does its Stream-K pieces first.
+//    whole, round-robin.
+// A CTA runs, in order: the Stream-K tiles lying entirely in its range; its contribution
+// (the start of its range, if that is inside a tile); the tile its range ends in, if it owns
+// that tile but does not finish it; then its whole tiles outside the Stream-K region.
 std::vector<Segment> schedule(int mode, int64_t tiles, int64_t iters, int64_t grid) {
   std::vector<Segment> out;
   if (mode == MODE_DP) {
@@ -171,10 +174,11 @@ std::vector<Segment> schedule(int mode, int64_t tiles, int64_t iters, int64_t gr
   const int64_t base = total / grid;
   const int64_t extra = total % grid;
   for (int64_t c = 0; c < grid; ++c) {
+    // cut this CTA's range at tile boundaries
     const int64_t begin = c * base + std::min(c, extra);
     const int64_t end = begin + base + (c < extra ? 1 : 0);
-    int64_t it = begin;
-    while (it < end) {
+    std::vector<Segment> pieces;
+    for (int64_t it = begin; it < end;) {
       const int64_t t = it / iters;
       const int64_t k0 = it % iters;
       const int64_t k1 = std::min(iters, k0 + (end - it));
@@ -182,9 +186,12 @@ std::vector<Segment> schedule(int mode, int64_t tiles, int64_t iters, int64_t gr
       if (k0 > 0) role = ROLE_CONTRIB;
       else if (k1 == iters) role = ROLE_FULL;
       else role = ROLE_OWNER;
-      out.push_back({c, whole_tiles + t, k0, k1, role});
+      pieces.push_back({c, whole_tiles + t, k0, k1, role});
       it += k1 - k0;
     }
+    for (const Segment& s : pieces) if (s.role == ROLE_FULL) out.push_back(s);
+    for (const Segment& s : pieces) if (s.role == ROLE_CONTRIB) out.push_back(s);
+    for (const Segment& s : pieces) if (s.role == ROLE_OWNER) out.push_back(s);
     for (int64_t t = c; t < whole_tiles; t += grid) out.push_back({c, t, 0, iters, ROLE_FULL});
   }
   return out;

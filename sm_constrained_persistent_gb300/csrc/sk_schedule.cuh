@@ -7,13 +7,14 @@
 //     flashinfer PR #982 "SM-constraint-GEMM by triton persistent kernel");
 //   * linear tiles [whole_tiles, tiles) form the Stream-K region: its tiles x iters
 //     iterations, in tile-major order, are cut into g contiguous ranges, CTA c's range holding
-//     sk_base iterations plus one if c < sk_extra.  Each CTA runs its Stream-K range first.
+//     sk_base iterations plus one if c < sk_extra.
 // A piece holding k = 0 makes its CTA the tile's owner; a piece starting past k = 0 is a
 // partial that the owner adds in before the bias (tritonBLAS PR #67 "Fix StreamK Kernel
-// Bias", Technical Details).  Because ranges are contiguous, only a CTA's first piece can
-// start inside a tile, so a CTA spills at most once (one scratch slot per CTA, as in
-// tritonBLAS PR #74 "Stream-k mxfp4 kernel"), and an owner's split tile is its last Stream-K
-// piece, continued by CTAs c+1, c+2, ...
+// Bias", Technical Details).  Because ranges are contiguous, only the start of a range can lie
+// inside a tile, so a CTA spills at most once (one scratch slot per CTA, as in tritonBLAS PR
+// #74 "Stream-k mxfp4 kernel"), and the tile a CTA owns but shares is the one its range ends
+// in, continued by CTAs c+1, c+2, ...  The order in which a CTA runs its pieces is given by
+// Cursor below.
 //
 // Linear tile index -> (tile row, tile column) goes through two bijections:
 //  1. In the Stream-K region, the tau-th tile owned by CTA c is given raster position
@@ -60,29 +61,69 @@ __host__ __device__ __forceinline__ int64_t sk_range_len(const Plan& p, int64_t 
   return p.sk_base + (cta < p.sk_extra ? 1 : 0);
 }
 
-// Walks one CTA's pieces in execution order.
+// Walks one CTA's pieces in execution order:
+//   1. the Stream-K tiles it owns entirely, in linear order,
+//   2. its contribution (the piece of its range that starts inside a tile), spilled to P,
+//   3. the tile it owns but shares (the piece of its range that ends inside a tile),
+//   4. its tiles of the whole-tile region (c, c+g, ...).
+// Contributions never wait, and every CTA reaches its contribution before its own shared
+// tile, so an owner's wait is short and there is no cycle.  Step 1 starts every tile at k = 0
+// on every CTA at the same time, so CTAs working on neighbouring tiles read the same k-slices
+// of A and B together; step 4 after the shared tile lets the owner's fix-up epilogue overlap
+// the next tile's main loop.
 struct Cursor {
-  int64_t it, end;   // remaining Stream-K iterations [it, end), relative to the region
-  int64_t next_whole;
+  int64_t begin, end;      // this CTA's Stream-K iterations [begin, end), region-relative
+  int64_t full_next, full_end;   // whole owned Stream-K tiles still to run (region tiles)
+  int64_t next_whole;      // next tile of the whole-tile region
+  int32_t step;            // 0: owned Stream-K tiles, 1: contribution, 2: shared owned
+                           // tile, 3: whole-tile region
 
   __host__ __device__ __forceinline__ Cursor(const Plan& p, int64_t cta) {
-    it = sk_range_begin(p, cta);
-    end = it + sk_range_len(p, cta);
+    begin = sk_range_begin(p, cta);
+    end = begin + sk_range_len(p, cta);
+    const int64_t first_full = (begin + p.iters - 1) / p.iters;   // first tile starting in range
+    const int64_t last_full = end / p.iters;                      // tiles ending in range
+    full_next = first_full;
+    full_end = last_full > first_full ? last_full : first_full;
     next_whole = cta;
+    step = 0;
   }
 
   __host__ __device__ __forceinline__ bool next(const Plan& p, Unit& u) {
-    if (it < end) {
-      const int64_t t = it / p.iters;
-      const int32_t k0 = static_cast<int32_t>(it - t * p.iters);
-      const int64_t left = end - it;
-      const int32_t k1 = (left >= p.iters - k0) ? p.iters : k0 + static_cast<int32_t>(left);
-      u.tile = p.whole_tiles + t;
-      u.k0 = k0;
-      u.k1 = k1;
-      u.role = (k0 > 0) ? kRoleContrib : (k1 == p.iters ? kRoleFull : kRoleOwner);
-      it += k1 - k0;
-      return true;
+    if (step == 0) {
+      if (full_next < full_end) {
+        u.tile = p.whole_tiles + full_next;
+        u.k0 = 0;
+        u.k1 = p.iters;
+        u.role = kRoleFull;
+        ++full_next;
+        return true;
+      }
+      step = 1;
+    }
+    if (step == 1) {
+      step = 2;
+      if (begin < end && begin % p.iters != 0) {   // starts inside a tile: a contribution
+        const int64_t t = begin / p.iters;
+        const int64_t tile_end = (t + 1) * p.iters;
+        u.tile = p.whole_tiles + t;
+        u.k0 = static_cast<int32_t>(begin - t * p.iters);
+        u.k1 = static_cast<int32_t>((end < tile_end ? end : tile_end) - t * p.iters);
+        u.role = kRoleContrib;
+        return true;
+      }
+    }
+    if (step == 2) {
+      step = 3;
+      // ends inside a tile whose k = 0 lies in this range: the shared tile this CTA owns
+      const int64_t t = end / p.iters;
+      if (begin < end && end % p.iters != 0 && t * p.iters >= begin) {
+        u.tile = p.whole_tiles + t;
+        u.k0 = 0;
+        u.k1 = static_cast<int32_t>(end - t * p.iters);
+        u.role = kRoleOwner;
+        return true;
+      }
     }
     if (next_whole < p.whole_tiles) {
       u.tile = next_whole;

@@ -183,7 +183,9 @@ def test_pair_streamk_wait_that_runs_out_reports_timeout():
     plan = sk.sk_plan(0, 2048, 256, 4096, 6, "streamk", 152, {"tile_m": 256})
     segs = sk.sk_plan_segments(plan)
     assert plan.ctas_per_tile == 2 and plan.grid == 3
-    assert segs[(segs[:, 0] == 1)][0, 4] == 2          # pair 1 starts with a contribution
+    contrib = segs[(segs[:, 0] == 1) & (segs[:, 4] == 2)]   # pair 1's contribution ...
+    owner = segs[(segs[:, 0] == 0) & (segs[:, 4] == 1)]     # ... to the tile pair 0 shares
+    assert len(contrib) == 1 and len(owner) == 1 and contrib[0, 1] == owner[0, 1]
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         sk.gemm_bf16(a, b, bias, mode="streamk", num_sms=6, stream=s,

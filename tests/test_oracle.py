@@ -357,6 +357,7 @@ def test_mxfp4_sampled_elements_agree_with_full():
 
 def _check_schedule(mode, T, I, g):
     segs = oracle.schedule(mode, T, I, g)
+    whole = {oracle.MODE_STREAMK: 0, oracle.MODE_HYBRID: T - T % g}.get(mode, T)
     cover = np.zeros((T, I), dtype=np.int64)
     owners = {}
     per_cta = {}
@@ -374,9 +375,22 @@ def _check_schedule(mode, T, I, g):
     assert set(owners) == set(range(T))
     for cta, lst in per_cta.items():
         contribs = [i for i, s in enumerate(lst) if s[3] == oracle.ROLE_CONTRIB]
-        assert contribs in ([], [0]), "a CTA spills at most once, and only its first piece"
         owned = [i for i, s in enumerate(lst) if s[3] == oracle.ROLE_OWNER]
+        assert len(contribs) <= 1, "a CTA spills at most once"
         assert len(owned) <= 1
+        # execution order: the Stream-K region's whole tiles, then the contribution, then
+        # the shared owned tile, then the tiles of the whole-tile region
+        region = [s for s in lst if s[0] >= whole]
+        order = [s[3] for s in region]
+        assert order == sorted(order, key=lambda r: {oracle.ROLE_FULL: 0, oracle.ROLE_CONTRIB: 1,
+                                                      oracle.ROLE_OWNER: 2}[r])
+        assert lst[:len(region)] == region
+        # the contribution is the start of the CTA's range: it precedes every other piece
+        # of the range in linear order
+        if contribs:
+            t, k0, k1, _ = lst[contribs[0]]
+            assert all((tt, kk0) > (t, k0) for tt, kk0, _, rr in lst if rr != oracle.ROLE_CONTRIB
+                       and tt >= t)
     # contributions of a split tile come from the CTAs right after the owner, in order
     for tile, (owner, k1, role) in owners.items():
         if role != oracle.ROLE_OWNER:
