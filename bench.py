@@ -186,14 +186,17 @@ class ClockSampler:
                 "samples": len(sms)}
 
 
-def tile_efficiency(plan, sm_count):
-    """Tile-quantisation efficiency: useful k-iterations / (SMs used x busiest SM's iterations)."""
+def tile_efficiency(plan, sm_count, num_sms=0):
+    """Tile-quantisation efficiency: useful k-iterations / (workers the call may use x the
+    busiest worker's iterations).  Workers are SMs, or SM pairs for pair tiles; the call may
+    use num_sms SMs (all when <= 0)."""
     import sm_constrained_persistent_gb300 as sk
     segs = sk.sk_plan_segments(plan)
     per_cta = np.zeros(plan.grid, dtype=np.int64)
     np.add.at(per_cta, segs[:, 0], segs[:, 3] - segs[:, 2])
     total = int(per_cta.sum())
-    slots = sm_count // plan.ctas_per_tile   # workers that run at once: SMs, or SM pairs
+    sms = sm_count if num_sms <= 0 or num_sms > sm_count else num_sms
+    slots = max(1, sms // plan.ctas_per_tile)
     if plan.grid > slots:      # data-parallel: workers run in waves of one per slot
         per_slot = np.zeros(slots, dtype=np.int64)
         np.add.at(per_slot, np.arange(plan.grid) % slots, per_cta)
@@ -427,7 +430,7 @@ def run_ours(args):
                    "bias": prob.p["bias"] is not None, "mode": args.mode,
                    "num_sms": args.num_sms if args.num_sms > 0 else sm_count,
                    "grid": plan.grid, "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}",
-                   "tile_quant_eff": round(tile_efficiency(plan, sm_count), 4),
+                   "tile_quant_eff": round(tile_efficiency(plan, sm_count, args.num_sms), 4),
                    "pct_of_dense_peak": round(100 * value / world / peak, 2),
                    "l2": ("L2 flushed before each step (256 MiB write)" if needs_flush(prob)
                           else "inputs larger than L2 (no flush)"),
@@ -461,7 +464,7 @@ def _time_modes(pr, modes, sm_count, peak, dist, num_sms=0, options=None, steps=
                      "pct_peak": round(100 * tflops / peak, 1), "grid": plan.grid,
                      "ctas": plan.grid * plan.ctas_per_tile,
                      "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}",
-                     "tile_quant_eff": round(tile_efficiency(plan, sm_count), 4)}
+                     "tile_quant_eff": round(tile_efficiency(plan, sm_count, num_sms), 4)}
     return res
 
 
