@@ -406,7 +406,8 @@ def run_ours(args):
         peak_note = f"fp4 dense = {peak_src} bf16 burst x {FP4_OVER_BF16:g} (nominal ratio)"
     gemm_ms = statistics.mean(per)   # one GEMM kernel dominates each call
     achieved = prob.flops / (gemm_ms * 1e-3) / 1e12
-    kernel_key = f"gemm_kernel<{'mxf4' if prob.fmt != 'bf16' else 'bf16'},{plan.tile_n}>:{args.workload}:{args.mode}"
+    kernel_key = (f"gemm<{'mxfp4' if prob.fmt != 'bf16' else 'bf16'},{plan.tile_m}x{plan.tile_n}>"
+                  f":{args.workload}:{args.mode}")
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                 "traffic": recorded_traffic(kernel_key), "peak_source": peak_note,

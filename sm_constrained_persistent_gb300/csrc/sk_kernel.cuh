@@ -270,7 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && cur.next(plan, u)) {
         int32_t tm, tn;
         tile_coords(plan, u.tile, tm, tn);
-        for (int32_t k = u.k0; k < u.k1; ++k) {
+        for (int32_t i = 0; i < u.k1 - u.k0; ++i) {
+          const int32_t k = unit_k(u, i);
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, args, kSiteProducer)) {
             ok = false;
             break;
@@ -330,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * Cf::kAccCols;
-        for (int32_t k = u.k0; k < u.k1; ++k) {
+        for (int32_t i = 0; i < u.k1 - u.k0; ++i) {
+          const int32_t k = unit_k(u, i);
           if (!wait_bar(&full[stage], phase, abort_flag, args, kSiteMma)) {
             ok = false;
             break;
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t ad = smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
               const uint64_t bd = smem_desc(b0 + j * 32, 16, 1024, kLayoutSwizzle128B);
               mma_mxf4(d_tmem, ad, bd, idesc, sfa_t + g * 4, sfb_t + g * (kBN / 32),
-                       (k > u.k0 || j > 0) ? 1u : 0u);
+                       (i > 0 || j > 0) ? 1u : 0u);
             }
           } else {
 #pragma unroll
@@ -372,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               //    8-row K groups 1024 B apart (stride offset); K advances 16 rows = 2 KB.
               const uint64_t ad = smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
               const uint64_t bd = smem_desc(b0 + j * 2048, 8192, 1024, kLayoutSwizzle128B);
-              mma_f16(d_tmem, ad, bd, Cf::kIdesc, (k > u.k0 || j > 0) ? 1u : 0u);
+              mma_f16(d_tmem, ad, bd, Cf::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
             }
           }
           mma_commit(&empty[stage]);

@@ -244,7 +244,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
         tile_coords(plan, u.tile, tm, tn);
         const int32_t row0 = tm * 256 + static_cast<int32_t>(rank) * 128;
         const int32_t col0 = tn * kBN + static_cast<int32_t>(rank) * Cf::kHalfN;
-        for (int32_t k = u.k0; k < u.k1; ++k) {
+        for (int32_t i = 0; i < u.k1 - u.k0; ++i) {
+          const int32_t k = unit_k(u, i);
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, args, kSiteProducer)) {
             ok = false;
             break;
@@ -302,7 +303,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * Cf::kAccCols;
-        for (int32_t k = u.k0; k < u.k1; ++k) {
+        for (int32_t i = 0; i < u.k1 - u.k0; ++i) {
+          const int32_t k = unit_k(u, i);
           // MXFP4: the scales-ready barrier also implies the stage's data has landed.
           if (!wait_bar(kMx ? &sf_ready[stage] : &full[stage], phase, abort_flag, args,
                         kSiteMma)) {
@@ -324,14 +326,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
               const uint64_t ad = smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
               const uint64_t bd = smem_desc(b0 + j * 32, 16, 1024, kLayoutSwizzle128B);
               mma_mxf4_pair(d_tmem, ad, bd, idesc, sfa_t + g * 4, sfb_t + g * 8,
-                            (k > u.k0 || j > 0) ? 1u : 0u);
+                            (i > 0 || j > 0) ? 1u : 0u);
             }
           } else {
 #pragma unroll
             for (int j = 0; j < Cf::kMmasPerStage; ++j) {
               const uint64_t ad = smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
               const uint64_t bd = smem_desc(b0 + j * 2048, 8192, 1024, kLayoutSwizzle128B);
-              mma_f16_pair(d_tmem, ad, bd, Cf::kIdesc, (k > u.k0 || j > 0) ? 1u : 0u);
+              mma_f16_pair(d_tmem, ad, bd, Cf::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
             }
           }
           mma_commit_pair(&empty[stage]);
@@ -360,7 +362,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
         Cursor cur(plan, pair);
         Unit u;
         while (ok && cur.next(plan, u)) {
-          for (int32_t k = u.k0; k < u.k1; ++k) {
+          for (int32_t i = 0; i < u.k1 - u.k0; ++i) {
+          const int32_t k = unit_k(u, i);
             if (!wait_bar(&full[stage], phase, abort_flag, args, kSiteMma)) {
               ok = false;
               break;

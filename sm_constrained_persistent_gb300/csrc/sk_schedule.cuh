@@ -137,6 +137,16 @@ struct Cursor {
   }
 };
 
+// The i-th k-iteration a piece runs.  Whole tiles ascend from k = 0; the two split pieces
+// (contribution and shared owned tile) descend from their last iteration.  CTAs reach their
+// split pieces at different times, and descending keeps them on neighbouring k-slices of A
+// and B at the same time: every contribution ends at the tile's last iteration, so they all
+// start there, and an owned piece picks up where the CTA's range ends.  Only the order of the
+// fp32 additions inside a piece changes.
+__host__ __device__ __forceinline__ int32_t unit_k(const Unit& u, int32_t i) {
+  return u.role == kRoleFull ? u.k0 + i : u.k1 - 1 - i;
+}
+
 // Raster position of a linear tile (bijection 1 above).
 __host__ __device__ __forceinline__ int64_t raster_position(const Plan& p, int64_t t) {
   if (t < p.whole_tiles) return t;
