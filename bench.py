@@ -469,6 +469,60 @@ def _time_modes(pr, modes, sm_count, peak, dist, num_sms=0, options=None, steps=
     return res
 
 
+def corun(pr, sm_count, gemm_calls=5, copy_bytes=256 << 20):
+    """The SM-constrained GEMM (persistent and Stream-K on half the SMs) beside a memory-bound
+    copy on a second stream: each stream's throughput alone and together (events per stream).
+    This is the intra-device sharing the num_sms cap exists for."""
+    import torch
+    half = sm_count // 2
+    src = torch.ones(copy_bytes // 4, dtype=torch.float32, device=pr.device)
+    dst = torch.empty_like(src)
+    s_gemm, s_copy = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def run(do_gemm, do_copy, mode, copies):
+        ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for k in ("gemm", "copy")}
+        torch.cuda.synchronize()
+        if do_copy:
+            with torch.cuda.stream(s_copy):
+                ev["copy"][0].record(s_copy)
+                for _ in range(copies):
+                    dst.copy_(src)
+                ev["copy"][1].record(s_copy)
+        if do_gemm:
+            with torch.cuda.stream(s_gemm):
+                ev["gemm"][0].record(s_gemm)
+                for _ in range(gemm_calls):
+                    pr.call(mode, half, s_gemm.cuda_stream)
+                ev["gemm"][1].record(s_gemm)
+        torch.cuda.synchronize()
+        res = {}
+        if do_gemm:
+            ms = ev["gemm"][0].elapsed_time(ev["gemm"][1]) / gemm_calls
+            res["gemm_tflops"] = round(pr.flops / (ms * 1e-3) / 1e12, 1)
+        if do_copy:
+            ms = ev["copy"][0].elapsed_time(ev["copy"][1]) / copies
+            res["copy_gbs"] = round(2 * copy_bytes / (ms * 1e-3) / 1e9, 1)
+        return res
+
+    out = {"num_sms": half, "copy": f"{copy_bytes >> 20} MiB device-to-device copies"}
+    for mode in ("persistent", "streamk"):
+        run(True, False, mode, 0)                               # warm-up
+        alone = run(True, False, mode, 0)
+        gemm_ms = pr.flops / (alone["gemm_tflops"] * 1e12) * 1e3 * gemm_calls
+        copy_alone = run(False, True, mode, 20)
+        per_copy_ms = 2 * copy_bytes / (copy_alone["copy_gbs"] * 1e9) * 1e3
+        copies = max(4, int(gemm_ms / per_copy_ms))             # both streams busy as long
+        both = run(True, True, mode, copies)
+        out[mode] = {"gemm_alone_tflops": alone["gemm_tflops"],
+                     "copy_alone_gbs": copy_alone["copy_gbs"],
+                     "gemm_corun_tflops": both["gemm_tflops"], "copy_corun_gbs": both["copy_gbs"]}
+    assert_ok = __import__("sm_constrained_persistent_gb300").sk_stream_status(s_gemm.cuda_stream)
+    if assert_ok != 0:
+        raise RuntimeError("co-run GEMM reported an error")
+    return out
+
+
 def extras(prob, sm_count, dist):
     """Per-schedule throughput of the benchmark workloads, each timed on its own after the
     headline region (3 warm-up + 10 timed calls per entry), and the SM-constrained sweep."""
@@ -512,6 +566,7 @@ def extras(prob, sm_count, dist):
             rows[str(ns)] = r
         sweep[name] = rows
     out["num_sms_sweep_persistent"] = sweep
+    out["corun_half_sms"] = corun(get("addmm_bf16_8192"), sm_count)
     for name in list(cache):
         if cache[name] is not prob:
             del cache[name]
