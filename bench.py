@@ -523,6 +523,45 @@ def corun(pr, sm_count, gemm_calls=5, copy_bytes=256 << 20):
     return out
 
 
+def backward(pr, bf16_peak, steps=10, warmup=3):
+    """The addmm backward of the 8192^3 workload (dA = dC B^T, dB = A^T dC, dbias), bf16
+    gradients, Stream-K: 4 M N K FLOPs per call (the column sum is not counted)."""
+    import torch
+    import sm_constrained_persistent_gb300 as sk
+    M, N, K = pr.M, pr.N, pr.K
+    dc = torch.randn((M, N), device=pr.device).to(torch.bfloat16)
+    a, b = pr.dev["A"], pr.dev["B"]
+    da = torch.empty((M, K), dtype=torch.bfloat16, device=pr.device)
+    db = torch.empty((K, N), dtype=torch.bfloat16, device=pr.device)
+    dbias = torch.empty((N,), dtype=torch.bfloat16, device=pr.device)
+    stream = torch.cuda.current_stream()
+
+    def call(mode):
+        return sk.sk_addmm_backward_bf16(dc.data_ptr(), a.data_ptr(), b.data_ptr(), da.data_ptr(),
+                                         db.data_ptr(), dbias.data_ptr(), sk.SK_BF16, M, N, K, 0,
+                                         sk.MODES[mode], stream.cuda_stream)
+
+    res = {}
+    for mode in ("streamk", "hybrid"):
+        for _ in range(warmup):
+            if call(mode) != 0:
+                raise RuntimeError("backward call failed")
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(steps):
+            call(mode)
+        e.record(stream)
+        torch.cuda.synchronize()
+        if sk.sk_stream_status(stream.cuda_stream) != 0:
+            raise RuntimeError("backward reported an error")
+        ms = s.elapsed_time(e) / steps
+        tflops = 4.0 * M * N * K / (ms * 1e-3) / 1e12
+        res[mode] = {"ms": round(ms, 4), "tflops": round(tflops, 1),
+                     "pct_peak": round(100 * tflops / bf16_peak, 1)}
+    return res
+
+
 def extras(prob, sm_count, dist):
     """Per-schedule throughput of the benchmark workloads, each timed on its own after the
     headline region (3 warm-up + 10 timed calls per entry), and the SM-constrained sweep."""
@@ -567,6 +606,7 @@ def extras(prob, sm_count, dist):
         sweep[name] = rows
     out["num_sms_sweep_persistent"] = sweep
     out["corun_half_sms"] = corun(get("addmm_bf16_8192"), sm_count)
+    out["addmm_backward_bf16_8192"] = backward(get("addmm_bf16_8192"), bpeak)
     for name in list(cache):
         if cache[name] is not prob:
             del cache[name]

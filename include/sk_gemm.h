@@ -143,6 +143,37 @@ sk_status_t sk_gemm_mxfp4_ex(const void* A, const void* A_scale, const void* B,
                              sk_mode_t mode, const sk_options_t* options, void* stream);
 
 /*
+ * sk_gemm_bf16_t — C[M x N] = op(A) * op(B) (+ bias[N]) with either bf16 operand stored
+ * transposed, through the same schedules and kernels (operands read M-major / K-major by the
+ * tensor cores, no copy).
+ *   trans_a = 0: A is M x K row-major;  trans_a = 1: A is stored K x M row-major (op(A) = A^T).
+ *   trans_b = 0: B is K x N row-major;  trans_b = 1: B is stored N x K row-major (op(B) = B^T).
+ *   Row pitches of the stored A and B (and N) must be multiples of 8 elements.  Other
+ *   arguments as sk_gemm_bf16_ex.
+ */
+sk_status_t sk_gemm_bf16_t(const void* A, int trans_a, const void* B, int trans_b,
+                           const void* bias, void* C, sk_dtype_t out_dtype, int64_t M, int64_t N,
+                           int64_t K, int num_sms, sk_mode_t mode, const sk_options_t* options,
+                           void* stream);
+
+/*
+ * sk_addmm_backward_bf16 — gradients of C = A * B + bias for an incoming gradient dC
+ * (the backward of the addmm the correctness tests of tritonBLAS PR #67 "Fix StreamK Kernel
+ * Bias" check through a.grad, b.grad and bias.grad):
+ *   dA = dC * B^T   (M x K),   dB = A^T * dC   (K x N),   dbias[n] = sum_m dC[m][n]   (N).
+ *   dC: M x N bf16; A: M x K bf16; B: K x N bf16 (the forward operands, as sk_gemm_bf16 takes
+ *   them).  dA, dB, dbias: outputs of grad_dtype (SK_BF16 or SK_F32); each may be NULL to skip
+ *   it (A may then be NULL when dB is skipped, B when dA is skipped).
+ *   The two GEMMs run with `mode` and `num_sms` like the forward; dbias is a column sum with
+ *   fp32 accumulation (deterministic, partial sums in the stream's workspace).
+ *   N and K must be multiples of 8, and M too when dB is requested.
+ */
+sk_status_t sk_addmm_backward_bf16(const void* dC, const void* A, const void* B, void* dA,
+                                   void* dB, void* dbias, sk_dtype_t grad_dtype, int64_t M,
+                                   int64_t N, int64_t K, int num_sms, sk_mode_t mode,
+                                   void* stream);
+
+/*
  * sk_gemm_bf16_static — sk_gemm_bf16 for callers that cannot allocate device memory.
  * The pages this library follows have no counterpart to this entry point.
  * Some callers may not allocate at the point where they run the GEMM (they live under an

@@ -78,6 +78,14 @@ def _lib():
             lib.oracle_addmm_bf16_scheduled.restype = i32
             lib.oracle_addmm_bf16_scheduled.argtypes = [vp, vp, vp, i32, i64, i64, i64, i32,
                                                         i64, i64, i64, i64, vp]
+            lib.oracle_gemm_bf16_t_rows.restype = i32
+            lib.oracle_gemm_bf16_t_rows.argtypes = [vp, i32, vp, i32, vp, i32, i64, i64, i64, i64,
+                                                    i64, vp, i32]
+            lib.oracle_gemm_bf16_t_at.restype = i32
+            lib.oracle_gemm_bf16_t_at.argtypes = [vp, i32, vp, i32, i64, i64, i64, vp, vp, i64, vp,
+                                                  i32]
+            lib.oracle_addmm_backward_bf16.restype = i32
+            lib.oracle_addmm_backward_bf16.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, i32]
             lib.oracle_hardware_threads.restype = i32
             lib.oracle_hardware_threads.argtypes = []
             _handle = lib
@@ -195,6 +203,52 @@ def addmm_mxfp4_at(A, A_scale, B, B_scale, bias, ms, ns, threads=0):
     if rc:
         raise ValueError(f"oracle_addmm_mxfp4_at failed ({rc})")
     return out
+
+
+def gemm_bf16_t(A, trans_a, B, trans_b, bias=None, rows=None, threads=0):
+    """binary64 op(A) @ op(B) (+ bias): A stored (M,K), or (K,M) when trans_a; B stored (K,N),
+    or (N,K) when trans_b; bf16 bits as uint16."""
+    A, B = _c(A, np.uint16), _c(B, np.uint16)
+    M, K = (A.shape[1], A.shape[0]) if trans_a else A.shape
+    N, K2 = (B.shape[0], B.shape[1]) if trans_b else (B.shape[1], B.shape[0])
+    assert K == K2
+    bias, bdt = _bias(bias)
+    m0, m1 = rows if rows is not None else (0, M)
+    out = np.empty((m1 - m0, N), dtype=np.float64)
+    rc = _lib().oracle_gemm_bf16_t_rows(_ptr(A), int(bool(trans_a)), _ptr(B), int(bool(trans_b)),
+                                        _ptr(bias), bdt, M, N, K, m0, m1, _ptr(out), threads)
+    if rc:
+        raise ValueError(f"oracle_gemm_bf16_t_rows failed ({rc})")
+    return out
+
+
+def gemm_bf16_t_at(A, trans_a, B, trans_b, ms, ns, threads=0):
+    A, B = _c(A, np.uint16), _c(B, np.uint16)
+    M, K = (A.shape[1], A.shape[0]) if trans_a else A.shape
+    N = B.shape[0] if trans_b else B.shape[1]
+    ms, ns = _c(ms, np.int64), _c(ns, np.int64)
+    out = np.empty(ms.shape, dtype=np.float64)
+    rc = _lib().oracle_gemm_bf16_t_at(_ptr(A), int(bool(trans_a)), _ptr(B), int(bool(trans_b)),
+                                      M, N, K, _ptr(ms), _ptr(ns), ms.size, _ptr(out), threads)
+    if rc:
+        raise ValueError(f"oracle_gemm_bf16_t_at failed ({rc})")
+    return out
+
+
+def addmm_backward_bf16(dC, A, B, threads=0):
+    """(dA, dB, dbias) in binary64 for C = A @ B + bias, given dC; bf16 bits as uint16."""
+    dC, A, B = _c(dC, np.uint16), _c(A, np.uint16), _c(B, np.uint16)
+    M, K = A.shape
+    N = B.shape[1]
+    assert dC.shape == (M, N) and B.shape == (K, N)
+    dA = np.empty((M, K), dtype=np.float64)
+    dB = np.empty((K, N), dtype=np.float64)
+    db = np.empty(N, dtype=np.float64)
+    rc = _lib().oracle_addmm_backward_bf16(_ptr(dC), _ptr(A), _ptr(B), M, N, K, _ptr(dA),
+                                           _ptr(dB), _ptr(db), threads)
+    if rc:
+        raise ValueError(f"oracle_addmm_backward_bf16 failed ({rc})")
+    return dA, dB, db
 
 
 def schedule(mode, tiles, iters, grid):

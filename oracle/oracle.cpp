@@ -30,6 +30,9 @@
 //  * scales are row-major [rows][K/32] bytes, block j covering k in [32j, 32j+32);
 //  * bias has the output's dtype (fp32 or bf16); a null bias means no bias.
 //  * Stream-K split: see oracle_schedule below.
+//  * addmm backward (the tests of tritonBLAS PR #67 compare a.grad, b.grad and bias.grad of
+//    addmm against torch): for C = A*B + bias and an incoming gradient dC,
+//    dA = dC * B^T, dB = A^T * dC, dbias[n] = sum over m of dC[m][n].
 
 #include <algorithm>
 #include <cmath>
@@ -254,6 +257,85 @@ int oracle_addmm_bf16_at(const uint16_t* A, const uint16_t* B, const void* bias,
     for (int64_t k = 0; k < K; ++k) s = s + bf16_value(A[m * K + k]) * bf16_value(B[k * N + n]);
     out[i] = s + bias_value(bias, bias_dtype, n);
   });
+  return 0;
+}
+
+// ---- general bf16 GEMM with stored-transposed operands ---------------------------------
+// C[m][n] = sum_k opA(m, k) * opB(k, n) (+ bias[n]), where opA(m, k) = A[m*K + k] (A stored
+// M x K) or A[k*M + m] when trans_a (A stored K x M), and opB(k, n) = B[k*N + n] (B stored
+// K x N) or B[n*K + k] when trans_b (B stored N x K).  Rows [m0, m1) into out.
+int oracle_gemm_bf16_t_rows(const uint16_t* A, int trans_a, const uint16_t* B, int trans_b,
+                            const void* bias, int bias_dtype, int64_t M, int64_t N, int64_t K,
+                            int64_t m0, int64_t m1, double* out, int threads) {
+  if (M < 0 || N < 0 || K < 0 || m0 < 0 || m1 > M || m0 > m1) return 1;
+  std::vector<double> Bv(static_cast<size_t>(K * N));   // opB(k, n) at k * N + n
+  for (int64_t k = 0; k < K; ++k)
+    for (int64_t n = 0; n < N; ++n)
+      Bv[k * N + n] = bf16_value(trans_b ? B[n * K + k] : B[k * N + n]);
+  parallel_rows(m0, m1, threads, [&](int64_t m) {
+    double* row = out + (m - m0) * N;
+    for (int64_t n = 0; n < N; ++n) row[n] = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      const double a = bf16_value(trans_a ? A[k * M + m] : A[m * K + k]);
+      const double* brow = Bv.data() + k * N;
+      for (int64_t n = 0; n < N; ++n) row[n] = row[n] + a * brow[n];
+    }
+    for (int64_t n = 0; n < N; ++n) row[n] = row[n] + bias_value(bias, bias_dtype, n);
+  });
+  return 0;
+}
+
+int oracle_gemm_bf16_t_at(const uint16_t* A, int trans_a, const uint16_t* B, int trans_b,
+                          int64_t M, int64_t N, int64_t K, const int64_t* ms, const int64_t* ns,
+                          int64_t count, double* out, int threads) {
+  for (int64_t i = 0; i < count; ++i)
+    if (ms[i] < 0 || ms[i] >= M || ns[i] < 0 || ns[i] >= N) return 1;
+  parallel_rows(0, count, threads, [&](int64_t i) {
+    const int64_t m = ms[i], n = ns[i];
+    double s = 0.0;
+    for (int64_t k = 0; k < K; ++k)
+      s = s + bf16_value(trans_a ? A[k * M + m] : A[m * K + k]) *
+                  bf16_value(trans_b ? B[n * K + k] : B[k * N + n]);
+    out[i] = s;
+  });
+  return 0;
+}
+
+// ---- addmm backward -------------------------------------------------------------------------
+// For C = A * B + bias (A: M x K, B: K x N, bf16) and dC (M x N, bf16):
+//   dA[m][k] = sum_n dC[m][n] * B[k][n]        (M x K)
+//   dB[k][n] = sum_m A[m][k] * dC[m][n]        (K x N)
+//   dbias[n] = sum_m dC[m][n]                  (N)
+// in binary64, sums in ascending index.  Any output pointer may be null.
+int oracle_addmm_backward_bf16(const uint16_t* dC, const uint16_t* A, const uint16_t* B,
+                               int64_t M, int64_t N, int64_t K, double* dA, double* dB,
+                               double* dbias, int threads) {
+  if (M < 1 || N < 1 || K < 1) return 1;
+  if (dA != nullptr) {
+    parallel_rows(0, M, threads, [&](int64_t m) {
+      for (int64_t k = 0; k < K; ++k) {
+        double s = 0.0;
+        for (int64_t n = 0; n < N; ++n) s = s + bf16_value(dC[m * N + n]) * bf16_value(B[k * N + n]);
+        dA[m * K + k] = s;
+      }
+    });
+  }
+  if (dB != nullptr) {
+    parallel_rows(0, K, threads, [&](int64_t k) {
+      for (int64_t n = 0; n < N; ++n) dB[k * N + n] = 0.0;
+      for (int64_t m = 0; m < M; ++m) {
+        const double a = bf16_value(A[m * K + k]);
+        for (int64_t n = 0; n < N; ++n) dB[k * N + n] = dB[k * N + n] + a * bf16_value(dC[m * N + n]);
+      }
+    });
+  }
+  if (dbias != nullptr) {
+    for (int64_t n = 0; n < N; ++n) {
+      double s = 0.0;
+      for (int64_t m = 0; m < M; ++m) s = s + bf16_value(dC[m * N + n]);
+      dbias[n] = s;
+    }
+  }
   return 0;
 }
 

@@ -81,6 +81,12 @@ def lib():
             h.sk_gemm_mxfp4_ex.restype = i32
             h.sk_gemm_mxfp4_ex.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, i32, i32,
                                            ctypes.POINTER(Options), vp]
+            h.sk_gemm_bf16_t.restype = i32
+            h.sk_gemm_bf16_t.argtypes = [vp, i32, vp, i32, vp, vp, i32, i64, i64, i64, i32, i32,
+                                         ctypes.POINTER(Options), vp]
+            h.sk_addmm_backward_bf16.restype = i32
+            h.sk_addmm_backward_bf16.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, i32,
+                                                 i32, vp]
             h.sk_gemm_bf16_static.restype = i32
             h.sk_gemm_bf16_static.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, i32, vp]
             h.sk_stream_status.restype = i32
@@ -134,6 +140,17 @@ def sk_gemm_mxfp4_ex(A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sm
                      options, stream):
     return lib().sk_gemm_mxfp4_ex(A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sms,
                                   mode, _opts(options), stream)
+
+
+def sk_gemm_bf16_t(A, trans_a, B, trans_b, bias, C, out_dtype, M, N, K, num_sms, mode, options,
+                   stream):
+    return lib().sk_gemm_bf16_t(A, trans_a, B, trans_b, bias, C, out_dtype, M, N, K, num_sms,
+                                mode, _opts(options), stream)
+
+
+def sk_addmm_backward_bf16(dC, A, B, dA, dB, dbias, grad_dtype, M, N, K, num_sms, mode, stream):
+    return lib().sk_addmm_backward_bf16(dC, A, B, dA, dB, dbias, grad_dtype, M, N, K, num_sms,
+                                        mode, stream)
 
 
 def sk_gemm_bf16_static(A, B, bias, C, out_dtype, M, N, K, num_sms, mode, stream):
@@ -249,6 +266,45 @@ def gemm_mxfp4(a, a_scale, b, b_scale, bias=None, out=None, out_dtype=None, num_
                           M, N, K, num_sms, _mode(mode), options, _stream_ptr(stream))
     _check(st, "sk_gemm_mxfp4")
     return out
+
+
+def gemm_bf16_t(a, b, trans_a=False, trans_b=False, bias=None, out=None, out_dtype=None,
+                num_sms=0, mode="streamk", options=None, stream=None):
+    """op(a) @ op(b) (+ bias): a is (M,K), or (K,M) stored when trans_a; b is (K,N), or (N,K)
+    stored when trans_b.  bf16 CUDA tensors."""
+    import torch
+    M, K = (a.shape[1], a.shape[0]) if trans_a else a.shape
+    N = b.shape[0] if trans_b else b.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=a.device)
+    for t in (a, b, out) + ((bias,) if bias is not None else ()):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    od = SK_BF16 if out.dtype == torch.bfloat16 else SK_F32
+    st = sk_gemm_bf16_t(a.data_ptr(), int(bool(trans_a)), b.data_ptr(), int(bool(trans_b)),
+                        bias.data_ptr() if bias is not None else None, out.data_ptr(), od, M, N,
+                        K, num_sms, _mode(mode), options, _stream_ptr(stream))
+    _check(st, "sk_gemm_bf16_t")
+    return out
+
+
+def addmm_backward(dc, a, b, need=("a", "b", "bias"), grad_dtype=None, num_sms=0,
+                   mode="streamk", stream=None):
+    """(da, db, dbias) of c = a @ b + bias for bf16 CUDA tensors; entries not in `need` are
+    None."""
+    import torch
+    M, K = a.shape
+    N = b.shape[1]
+    dt = grad_dtype or torch.bfloat16
+    da = torch.empty((M, K), dtype=dt, device=dc.device) if "a" in need else None
+    db = torch.empty((K, N), dtype=dt, device=dc.device) if "b" in need else None
+    dbias = torch.empty((N,), dtype=dt, device=dc.device) if "bias" in need else None
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    st = sk_addmm_backward_bf16(dc.data_ptr(), a.data_ptr(), b.data_ptr(), ptr(da), ptr(db),
+                                ptr(dbias), SK_BF16 if dt == torch.bfloat16 else SK_F32, M, N, K,
+                                num_sms, _mode(mode), _stream_ptr(stream))
+    _check(st, "sk_addmm_backward_bf16")
+    return da, db, dbias
 
 
 def stream_status(stream=None):

@@ -144,6 +144,8 @@ struct Workspace {
   uint32_t* err = nullptr;     // 4 words
   uint8_t* sf = nullptr;
   size_t sf_bytes = 0;
+  float* red = nullptr;        // column-sum partials (bias gradient)
+  size_t red_bytes = 0;
   uint32_t epoch = 0;
 };
 
@@ -238,10 +240,10 @@ cudaError_t regrow(T** ptr, size_t* have, size_t need, cudaStream_t st) {
 
 // Caller holds g_mutex.  Grows the workspace of (dev, st) to at least the given sizes.
 sk_status_t ensure_workspace(int dev, cudaStream_t st, size_t P_bytes, size_t flag_count,
-                             size_t sf_bytes, Workspace** out) {
+                             size_t sf_bytes, Workspace** out, size_t red_bytes = 0) {
   Workspace& w = g_workspaces[{dev, st}];
   const bool fits = w.err != nullptr && w.P_bytes >= P_bytes && w.flag_count >= flag_count &&
-                    w.sf_bytes >= sf_bytes;
+                    w.sf_bytes >= sf_bytes && w.red_bytes >= red_bytes;
   if (!fits) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return SK_ERR_CUDA;
@@ -260,6 +262,7 @@ sk_status_t ensure_workspace(int dev, cudaStream_t st, size_t P_bytes, size_t fl
       if (cudaMemsetAsync(w.flags, 0, bytes, st) != cudaSuccess) return SK_ERR_CUDA;
     }
     if (sf_bytes > 0 && regrow(&w.sf, &w.sf_bytes, sf_bytes, st) != cudaSuccess) return SK_ERR_OOM;
+    if (red_bytes > 0 && regrow(&w.red, &w.red_bytes, red_bytes, st) != cudaSuccess) return SK_ERR_OOM;
   }
   *out = &w;
   return SK_OK;
@@ -298,7 +301,8 @@ bool encode_scale_rows(CUtensorMap* map, const void* base, int64_t row_blocks, i
 
 sk_status_t validate(int format, const void* A, const void* A_scale, const void* B,
                      const void* B_scale, const void* bias, const void* C, int out_dtype,
-                     int64_t M, int64_t N, int64_t K, int mode, const sk_options_t* opt) {
+                     int64_t M, int64_t N, int64_t K, int mode, const sk_options_t* opt,
+                     int layout = 0) {
   if (A == nullptr || B == nullptr || C == nullptr) return SK_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (bias && !aligned16(bias)))
     return SK_ERR_INVALID_ARG;
@@ -307,8 +311,12 @@ sk_status_t validate(int format, const void* A, const void* A_scale, const void*
   if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return SK_ERR_INVALID_ARG;
   if (format == 0) {
-    if (K % 8 != 0 || N % 8 != 0) return SK_ERR_INVALID_ARG;   // 16-byte row pitches
+    // 16-byte row pitches: A rows hold K (or M when stored transposed), B rows N (or K)
+    const int64_t a_pitch = (layout & 1) ? M : K;
+    const int64_t b_pitch = (layout & 2) ? K : N;
+    if (a_pitch % 8 != 0 || b_pitch % 8 != 0 || N % 8 != 0) return SK_ERR_INVALID_ARG;
   } else {
+    if (layout != 0) return SK_ERR_INVALID_ARG;
     if (A_scale == nullptr || B_scale == nullptr) return SK_ERR_INVALID_ARG;
     if (K % 32 != 0) return SK_ERR_INVALID_ARG;
   }
@@ -322,11 +330,13 @@ sk_status_t validate(int format, const void* A, const void* A_scale, const void*
   return SK_OK;
 }
 
+// layout: bit 0 = A stored transposed (K x M), bit 1 = B stored transposed (N x K); bf16 only.
 sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void* B,
                      const void* B_scale, const void* bias, void* C, sk_dtype_t out_dtype,
                      int64_t M, int64_t N, int64_t K, int num_sms, sk_mode_t mode,
-                     const sk_options_t* opt, void* stream_ptr) {
-  sk_status_t st = validate(format, A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, mode, opt);
+                     const sk_options_t* opt, void* stream_ptr, int layout = 0) {
+  sk_status_t st =
+      validate(format, A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, mode, opt, layout);
   if (st != SK_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   int dev = 0;
@@ -338,17 +348,19 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   if (di->cc_major != 10 || di->cc_minor != 3) return SK_ERR_UNSUPPORTED;   // built for sm_103a
 
   // The pair variants' cluster capacity is needed to plan; set both candidates up first.
-  const int pair_variant = format == 1 ? sk::kVariantMxPair : sk::kVariantBf16Pair;
+  const int pair_variant = format == 1 ? sk::kVariantMxPair
+                                       : sk::variant_of(sk::kKindBf16Pair, layout);
   if ((st = ensure_variant(*di, pair_variant)) != SK_OK) return st;
   sk_plan_t plan;
   if ((st = make_plan(format, M, N, K, num_sms, mode, di->sm_count, di->max_pairs[pair_variant],
                       opt, &plan)) != SK_OK)
     return st;
   const bool pair = plan.ctas_per_tile == 2;
-  const int variant = pair ? pair_variant
-                           : (format == 1 ? sk::kVariantMxN128
-                                          : (plan.tile_n == 256 ? sk::kVariantBf16N256
-                                                                : sk::kVariantBf16N128));
+  const int variant =
+      pair ? pair_variant
+           : (format == 1 ? sk::kVariantMxN128
+                          : sk::variant_of(plan.tile_n == 256 ? sk::kKindBf16N256 : sk::kKindBf16N128,
+                                           layout));
   if ((st = ensure_variant(*di, variant)) != SK_OK) return st;
   const bool streamk = plan.sk_tiles > 0;
   if (streamk) {
@@ -372,8 +384,13 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   const uint32_t b_box = pair ? 128u : static_cast<uint32_t>(plan.tile_n);   // B rows per CTA (MXFP4)
   bool ok;
   if (format == 0) {
-    ok = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, M, K, 64, kTileM) &&
-         encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, 64, 64);
+    // A: M x K (box 64 k x 128 rows), or stored K x M (box 64 m x 64 k-rows).
+    // B: K x N (box 64 n x 64 k-rows), or stored N x K (box 64 k x one CTA's columns).
+    const uint32_t bt_rows = pair ? 128u : static_cast<uint32_t>(plan.tile_n);
+    ok = ((layout & 1) ? encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, 64, 64)
+                       : encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, M, K, 64, kTileM)) &&
+         ((layout & 2) ? encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, 64, bt_rows)
+                       : encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, 64, 64));
   } else {
     ok = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, M, K / 2, 128, kTileM) &&
          encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, N, K / 2, 128, b_box);
@@ -457,6 +474,60 @@ sk_status_t sk_gemm_mxfp4_ex(const void* A, const void* A_scale, const void* B,
                   stream);
 }
 
+sk_status_t sk_gemm_bf16_t(const void* A, int trans_a, const void* B, int trans_b,
+                           const void* bias, void* C, sk_dtype_t out_dtype, int64_t M, int64_t N,
+                           int64_t K, int num_sms, sk_mode_t mode, const sk_options_t* options,
+                           void* stream) {
+  if ((trans_a != 0 && trans_a != 1) || (trans_b != 0 && trans_b != 1)) return SK_ERR_INVALID_ARG;
+  return run_gemm(0, A, nullptr, B, nullptr, bias, C, out_dtype, M, N, K, num_sms, mode, options,
+                  stream, trans_a | (trans_b << 1));
+}
+
+sk_status_t sk_addmm_backward_bf16(const void* dC, const void* A, const void* B, void* dA,
+                                   void* dB, void* dbias, sk_dtype_t grad_dtype, int64_t M,
+                                   int64_t N, int64_t K, int num_sms, sk_mode_t mode,
+                                   void* stream) {
+  if (dC == nullptr || (dA == nullptr && dB == nullptr && dbias == nullptr))
+    return SK_ERR_INVALID_ARG;
+  if ((dA != nullptr && B == nullptr) || (dB != nullptr && A == nullptr)) return SK_ERR_INVALID_ARG;
+  if (grad_dtype != SK_F32 && grad_dtype != SK_BF16) return SK_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return SK_ERR_INVALID_ARG;
+  if (!aligned16(dC) || (dA && !aligned16(dA)) || (dB && !aligned16(dB)) ||
+      (dbias && !aligned16(dbias)) || (A && !aligned16(A)) || (B && !aligned16(B)))
+    return SK_ERR_INVALID_ARG;
+  if (N % 8 != 0 || K % 8 != 0) return SK_ERR_INVALID_ARG;
+  if (dB != nullptr && M % 8 != 0) return SK_ERR_INVALID_ARG;   // A read M-major
+  sk_status_t st = SK_OK;
+  // dA (M x K) = dC (M x N) * B^T: B is stored K x N, i.e. transposed for this product.
+  if (dA != nullptr &&
+      (st = run_gemm(0, dC, nullptr, B, nullptr, nullptr, dA, grad_dtype, M, K, N, num_sms, mode,
+                     nullptr, stream, 2)) != SK_OK)
+    return st;
+  // dB (K x N) = A^T * dC: A is stored M x K, i.e. transposed for this product.
+  if (dB != nullptr &&
+      (st = run_gemm(0, A, nullptr, dC, nullptr, nullptr, dB, grad_dtype, K, N, M, num_sms, mode,
+                     nullptr, stream, 1)) != SK_OK)
+    return st;
+  if (dbias != nullptr) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SK_ERR_UNSUPPORTED;
+    Workspace* ws = nullptr;
+    {
+      std::lock_guard<std::mutex> lock(g_mutex);
+      DeviceInfo* di = nullptr;
+      if ((st = device_info(dev, &di)) != SK_OK) return st;
+      if (di->cc_major != 10 || di->cc_minor != 3) return SK_ERR_UNSUPPORTED;
+      if ((st = ensure_workspace(dev, s, 0, 1, 0, &ws,
+                                 static_cast<size_t>(sk::colsum_scratch_bytes(M, N)))) != SK_OK)
+        return st;
+    }
+    if (sk::colsum_bf16(dC, M, N, dbias, grad_dtype == SK_BF16 ? 1 : 0, ws->red, s) != cudaSuccess)
+      return SK_ERR_CUDA;
+  }
+  return SK_OK;
+}
+
 sk_status_t sk_stream_status(void* stream_ptr) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   if (cudaStreamSynchronize(stream) != cudaSuccess) return SK_ERR_CUDA;
@@ -524,6 +595,7 @@ void sk_workspace_release_all(void) {
     if (w.flags) cudaFree(w.flags);
     if (w.err) cudaFree(w.err);
     if (w.sf) cudaFree(w.sf);
+    if (w.red) cudaFree(w.red);
   }
   g_workspaces.clear();
   cudaSetDevice(prev);
@@ -558,13 +630,16 @@ sk_status_t sk_device_caps(int device, sk_device_caps_t* caps) {
       caps->cc_major = d->cc_major;
       caps->cc_minor = d->cc_minor;
       if (d->cc_major == 10 && d->cc_minor == 3) {
-        for (int v = 0; v < sk::kNumVariants; ++v) ensure_variant(*d, v);
+        // the five reported variants, in the order of sk_device_caps_t's arrays
+        const int reported[5] = {sk::kVariantBf16N128, sk::kVariantBf16N256, sk::kVariantMxN128,
+                                 sk::kVariantBf16Pair, sk::kVariantMxPair};
+        for (int i = 0; i < 5; ++i) ensure_variant(*d, reported[i]);
         caps->ctas_per_sm[0] = d->ctas_per_sm[sk::kVariantBf16N128];
         caps->ctas_per_sm[1] = d->ctas_per_sm[sk::kVariantBf16N256];
         caps->ctas_per_sm[2] = d->ctas_per_sm[sk::kVariantMxN128];
         caps->max_pair_clusters[0] = d->max_pairs[sk::kVariantBf16Pair];
         caps->max_pair_clusters[1] = d->max_pairs[sk::kVariantMxPair];
-        for (int v = 0; v < sk::kNumVariants; ++v) caps->setup_error[v] = d->setup_error[v];
+        for (int i = 0; i < 5; ++i) caps->setup_error[i] = d->setup_error[reported[i]];
       } else {
         st = SK_ERR_UNSUPPORTED;
       }

@@ -52,9 +52,12 @@ enum : uint32_t {
 
 
 
-template <bool kMx, int kBN>
+// kAT: A is stored transposed (K x M row-major) and read M-major; kBT: B is stored transposed
+// (N x K row-major) and read K-major.  Both are bf16-only.
+template <bool kMx, int kBN, bool kAT = false, bool kBT = false>
 struct Cfg {
   static_assert(kBN == 128 || kBN == 256, "tile width");
+  static_assert(!kMx || (!kAT && !kBT), "MXFP4 operands are K-major");
   static_assert(!kMx || kBN == 128, "MXFP4 tiles are 128 wide");
   static constexpr int kTileK = kMx ? 256 : 64;        // K elements per k-iteration (128 B rows)
   static constexpr int kMmaK = kMx ? 64 : 16;          // K per tcgen05.mma
@@ -75,13 +78,14 @@ struct Cfg {
   static constexpr size_t kSmemBytes =
       1024 + static_cast<size_t>(kStages) * kStageBytes + kBarrierBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  // Instruction descriptor: fp32 D, K-major A; bf16: bf16 A/B, MN-major B;
-  // MXFP4: E2M1 A/B, E8M0 scales.  N >> 3 at bit 17, M >> 4 at bit 24.
+  // Instruction descriptor: fp32 D; bf16: bf16 A/B, A K-major (M-major when kAT, bit 15),
+  // B MN-major (K-major when kBT, bit 16 clear); MXFP4: E2M1 A/B, E8M0 scales, both K-major.
+  // N >> 3 at bit 17, M >> 4 at bit 24.
   static constexpr uint32_t kIdesc =
       kMx ? ((1u << 7) | (1u << 10) | (1u << 23) | (uint32_t(kBN >> 3) << 17) |
              (uint32_t(kBM >> 4) << 24))
-          : ((1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | (uint32_t(kBN >> 3) << 17) |
-             (uint32_t(kBM >> 4) << 24));
+          : ((1u << 4) | (1u << 7) | (1u << 10) | (kAT ? (1u << 15) : 0u) |
+             (kBT ? 0u : (1u << 16)) | (uint32_t(kBN >> 3) << 17) | (uint32_t(kBM >> 4) << 24));
 };
 
 __device__ __forceinline__ void record_error(const Args& a, uint32_t site, int64_t tile) {
@@ -204,11 +208,11 @@ __device__ __forceinline__ void store_row_chunk(const Args& a, int64_t m, int64_
   }
 }
 
-template <bool kMx, int kBN>
+template <bool kMx, int kBN, bool kAT = false, bool kBT = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ Args args) {
-  using Cf = Cfg<kMx, kBN>;
+  using Cf = Cfg<kMx, kBN, kAT, kBT>;
   constexpr int S = Cf::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -292,10 +296,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         args.sfb + (nb * args.sf_kgroups + 2 * k) * 512, 1024, &full[stage]);
             }
           } else {
-            tma_load_2d(sa, &tmA, &full[stage], k * 64, tm * kBM);
+            // A: K-major tile (rows x 64 k), or M-major (64 k-rows x 128 m, two 64-wide boxes).
+            if constexpr (kAT) {
+              tma_load_2d(sa, &tmA, &full[stage], tm * kBM, k * 64);
+              tma_load_2d(sa + 8192, &tmA, &full[stage], tm * kBM + 64, k * 64);
+            } else {
+              tma_load_2d(sa, &tmA, &full[stage], k * 64, tm * kBM);
+            }
+            // B: MN-major (64 k-rows x BN n, 64-wide boxes), or K-major (BN rows x 64 k).
+            if constexpr (kBT) {
+              tma_load_2d(sb, &tmB, &full[stage], k * 64, tn * kBN);
+            } else {
 #pragma unroll
-            for (int j = 0; j < kBN / 64; ++j)
-              tma_load_2d(sb + j * 8192, &tmB, &full[stage], tn * kBN + j * 64, k * 64);
+              for (int j = 0; j < kBN / 64; ++j)
+                tma_load_2d(sb + j * 8192, &tmB, &full[stage], tn * kBN + j * 64, k * 64);
+            }
           }
           ++issued;
           if (++stage == S) {
@@ -372,8 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; K advances 32 B.
               // B: MN-major, 128-byte swizzle; 64-column blocks 8 KB apart (leading offset),
               //    8-row K groups 1024 B apart (stride offset); K advances 16 rows = 2 KB.
-              const uint64_t ad = smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
-              const uint64_t bd = smem_desc(b0 + j * 2048, 8192, 1024, kLayoutSwizzle128B);
+              // M-major A / MN-major B: 64-wide blocks 8 KB apart, K advances 16 rows = 2 KB.
+              const uint64_t ad = kAT ? smem_desc(a0 + j * 2048, 8192, 1024, kLayoutSwizzle128B)
+                                      : smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
+              const uint64_t bd = kBT ? smem_desc(b0 + j * 32, 16, 1024, kLayoutSwizzle128B)
+                                      : smem_desc(b0 + j * 2048, 8192, 1024, kLayoutSwizzle128B);
               mma_f16(d_tmem, ad, bd, Cf::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
             }
           }

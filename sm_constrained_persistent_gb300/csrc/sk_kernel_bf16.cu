@@ -1,12 +1,13 @@
-// bf16 instantiations of the GEMM kernel (CTA tiles 128 x 128 and 128 x 256).
+// bf16 instantiations of the one-CTA-per-tile GEMM kernel, 128 x 128 tiles, all four
+// operand layouts.
 #include "sk_kernel.cuh"
 #include "sk_launch.h"
 
 namespace sk {
 
-template <bool kMx, int kBN>
-cudaError_t launch_variant(const Launch& l) {
-  using Cf = Cfg<kMx, kBN>;
+template <bool kAT, bool kBT>
+static cudaError_t launch_one(const Launch& l) {
+  using Cf = Cfg<false, 128, kAT, kBT>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(l.grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -17,31 +18,36 @@ cudaError_t launch_variant(const Launch& l) {
   attr[0].val.cooperative = l.cooperative ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<kMx, kBN>, *l.tmA, *l.tmB, l.args);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<false, 128, kAT, kBT>, *l.tmA, *l.tmB, l.args);
 }
 
-template <bool kMx, int kBN>
-cudaError_t setup_variant(int* ctas_per_sm) {
-  using Cf = Cfg<kMx, kBN>;
-  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kMx, kBN>,
+template <bool kAT, bool kBT>
+static cudaError_t setup_one(int* ctas_per_sm) {
+  using Cf = Cfg<false, 128, kAT, kBT>;
+  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<false, 128, kAT, kBT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cf::kSmemBytes));
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gemm_kernel<kMx, kBN>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gemm_kernel<false, 128, kAT, kBT>,
                                                        kThreads, Cf::kSmemBytes);
 }
 
-cudaError_t launch_bf16(int tile_n, const Launch& l) {
-  return tile_n == 256 ? launch_variant<false, 256>(l) : launch_variant<false, 128>(l);
+cudaError_t setup_bf16_n128(int layout, int* ctas_per_sm) {
+  switch (layout) {
+    case 1: return setup_one<true, false>(ctas_per_sm);
+    case 2: return setup_one<false, true>(ctas_per_sm);
+    case 3: return setup_one<true, true>(ctas_per_sm);
+    default: return setup_one<false, false>(ctas_per_sm);
+  }
 }
 
-cudaError_t setup_bf16(int tile_n, int* ctas_per_sm) {
-  return tile_n == 256 ? setup_variant<false, 256>(ctas_per_sm)
-                       : setup_variant<false, 128>(ctas_per_sm);
-}
-
-size_t smem_bf16(int tile_n) {
-  return tile_n == 256 ? Cfg<false, 256>::kSmemBytes : Cfg<false, 128>::kSmemBytes;
+cudaError_t launch_bf16_n128(int layout, const Launch& l) {
+  switch (layout) {
+    case 1: return launch_one<true, false>(l);
+    case 2: return launch_one<false, true>(l);
+    case 3: return launch_one<true, true>(l);
+    default: return launch_one<false, false>(l);
+  }
 }
 
 }  // namespace sk

@@ -1,12 +1,9 @@
 // MXFP4 instantiation of the GEMM kernel, the scale-layout kernel, and the variant dispatch.
 #include "sk_kernel.cuh"
+#include "sk_kernel_pair.cuh"
 #include "sk_launch.h"
 
 namespace sk {
-
-cudaError_t launch_bf16(int tile_n, const Launch& l);
-cudaError_t setup_bf16(int tile_n, int* ctas_per_sm);
-size_t smem_bf16(int tile_n);
 
 // One 128-thread block per 512-byte output group (row block rb, k group g): thread t writes
 // word t, i.e. scales (row rb*128 + 32*(t%4) + t/4, blocks 4g .. 4g+3).  blockIdx.y < a_blocks
@@ -50,40 +47,66 @@ cudaError_t mx_scale_prep(const uint8_t* a_scales, int64_t a_rows, int64_t a_row
 }
 
 size_t variant_smem_bytes(int variant) {
-  switch (variant) {
-    case kVariantBf16N128: return smem_bf16(128);
-    case kVariantBf16N256: return smem_bf16(256);
-    default: return Cfg<true, 128>::kSmemBytes;
+  switch (variant_kind(variant)) {
+    case kKindBf16N128: return Cfg<false, 128>::kSmemBytes;
+    case kKindBf16N256: return Cfg<false, 256>::kSmemBytes;
+    case kKindMxN128: return Cfg<true, 128>::kSmemBytes;
+    case kKindBf16Pair: return PairCfg<false>::kSmemBytes;
+    default: return PairCfg<true>::kSmemBytes;
   }
 }
 
 cudaError_t variant_setup(int variant, int* ctas_per_sm) {
-  if (variant == kVariantBf16N128) return setup_bf16(128, ctas_per_sm);
-  if (variant == kVariantBf16N256) return setup_bf16(256, ctas_per_sm);
-  using Cf = Cfg<true, 128>;
-  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<true, 128>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(Cf::kSmemBytes));
-  if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gemm_kernel<true, 128>,
-                                                       kThreads, Cf::kSmemBytes);
+  const int layout = variant_layout(variant);
+  switch (variant_kind(variant)) {
+    case kKindBf16N128: return setup_bf16_n128(layout, ctas_per_sm);
+    case kKindBf16N256: return setup_bf16_n256(layout, ctas_per_sm);
+    case kKindMxN128: {
+      using Cf = Cfg<true, 128>;
+      cudaError_t e = cudaFuncSetAttribute(gemm_kernel<true, 128>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(Cf::kSmemBytes));
+      if (e != cudaSuccess) return e;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gemm_kernel<true, 128>,
+                                                           kThreads, Cf::kSmemBytes);
+    }
+    default: return cudaErrorInvalidValue;   // pair kinds: pair_variant_setup
+  }
 }
 
 cudaError_t variant_launch(int variant, const Launch& l) {
-  if (variant == kVariantBf16N128) return launch_bf16(128, l);
-  if (variant == kVariantBf16N256) return launch_bf16(256, l);
-  using Cf = Cfg<true, 128>;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(l.grid), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cf::kSmemBytes;
-  cfg.stream = l.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = l.cooperative ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<true, 128>, *l.tmA, *l.tmB, l.args);
+  const int layout = variant_layout(variant);
+  switch (variant_kind(variant)) {
+    case kKindBf16N128: return launch_bf16_n128(layout, l);
+    case kKindBf16N256: return launch_bf16_n256(layout, l);
+    case kKindMxN128: {
+      using Cf = Cfg<true, 128>;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(l.grid), 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = Cf::kSmemBytes;
+      cfg.stream = l.stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = l.cooperative ? 1 : 0;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, gemm_kernel<true, 128>, *l.tmA, *l.tmB, l.args);
+    }
+    default: return cudaErrorInvalidValue;   // pair kinds: pair_variant_launch
+  }
 }
+
+cudaError_t pair_variant_setup(int variant, int* max_clusters) {
+  return variant_kind(variant) == kKindMxPair ? setup_mx_pair(max_clusters)
+                                              : setup_bf16_pair(variant_layout(variant), max_clusters);
+}
+
+cudaError_t pair_variant_launch(int variant, const Launch& l) {
+  return variant_kind(variant) == kKindMxPair ? launch_mx_pair(l)
+                                              : launch_bf16_pair(variant_layout(variant), l);
+}
+
+size_t pair_variant_smem_bytes(int variant) { return variant_smem_bytes(variant); }
 
 }  // namespace sk

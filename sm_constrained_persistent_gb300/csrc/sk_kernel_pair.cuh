@@ -127,8 +127,9 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-template <bool kMx>
+template <bool kMx, bool kAT = false, bool kBT = false>
 struct PairCfg {
+  static_assert(!kMx || (!kAT && !kBT), "MXFP4 operands are K-major");
   static constexpr int kBN = 256;                        // pair tile: 256 x 256
   static constexpr int kHalfN = kBN / 2;                 // B columns loaded by each CTA
   static constexpr int kTileK = kMx ? 256 : 64;
@@ -155,18 +156,18 @@ struct PairCfg {
   static constexpr uint32_t kIdesc =
       kMx ? ((1u << 7) | (1u << 10) | (1u << 23) | (uint32_t(kBN >> 3) << 17) |
              (uint32_t(256 >> 4) << 24))
-          : ((1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | (uint32_t(kBN >> 3) << 17) |
-             (uint32_t(256 >> 4) << 24));
+          : ((1u << 4) | (1u << 7) | (1u << 10) | (kAT ? (1u << 15) : 0u) |
+             (kBT ? 0u : (1u << 16)) | (uint32_t(kBN >> 3) << 17) | (uint32_t(256 >> 4) << 24));
 };
 
 // Registers are granted per 128-thread warpgroup, so 320 or 352 threads are charged as 384:
 // the launch bound caps the kernel at 65536 / 384 -> 168 registers per thread.
-template <bool kMx>
+template <bool kMx, bool kAT = false, bool kBT = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSfa,
                      const __grid_constant__ CUtensorMap tmSfb, const __grid_constant__ Args args) {
-  using Cf = PairCfg<kMx>;
+  using Cf = PairCfg<kMx, kAT, kBT>;
   constexpr int S = Cf::kStages;
   constexpr int kBN = Cf::kBN;
   extern __shared__ uint8_t smem_raw[];
@@ -266,9 +267,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
             tma_load_2d_pair(ring_sfb + stage * Cf::kStageSfb + 1024, &tmSfb, fb, 0,
                              (tn * 2 + 1) * plan.iters + k);
           } else {
-            tma_load_2d_pair(sa, &tmA, fb, k * 64, row0);
-            tma_load_2d_pair(sb, &tmB, fb, col0, k * 64);
-            tma_load_2d_pair(sb + 8192, &tmB, fb, col0 + 64, k * 64);
+            if constexpr (kAT) {   // M-major A: two 64-wide boxes of 64 k-rows
+              tma_load_2d_pair(sa, &tmA, fb, row0, k * 64);
+              tma_load_2d_pair(sa + 8192, &tmA, fb, row0 + 64, k * 64);
+            } else {
+              tma_load_2d_pair(sa, &tmA, fb, k * 64, row0);
+            }
+            if constexpr (kBT) {   // K-major B: this CTA's 128 columns as rows of 64 k
+              tma_load_2d_pair(sb, &tmB, fb, k * 64, col0);
+            } else {
+              tma_load_2d_pair(sb, &tmB, fb, col0, k * 64);
+              tma_load_2d_pair(sb + 8192, &tmB, fb, col0 + 64, k * 64);
+            }
           }
           ++issued;
           if (++stage == S) {
@@ -331,8 +341,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
           } else {
 #pragma unroll
             for (int j = 0; j < Cf::kMmasPerStage; ++j) {
-              const uint64_t ad = smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
-              const uint64_t bd = smem_desc(b0 + j * 2048, 8192, 1024, kLayoutSwizzle128B);
+              const uint64_t ad = kAT ? smem_desc(a0 + j * 2048, 8192, 1024, kLayoutSwizzle128B)
+                                      : smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
+              const uint64_t bd = kBT ? smem_desc(b0 + j * 32, 16, 1024, kLayoutSwizzle128B)
+                                      : smem_desc(b0 + j * 2048, 8192, 1024, kLayoutSwizzle128B);
               mma_f16_pair(d_tmem, ad, bd, Cf::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
             }
           }

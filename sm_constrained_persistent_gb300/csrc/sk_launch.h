@@ -8,18 +8,34 @@
 
 namespace sk {
 
-// Kernel variants: operand format x CTA tile.  The pair variants run 2-CTA clusters on
-// 256 x 256 tiles (one CTA per 128 rows); `Launch::grid` always counts CTAs.
-enum Variant : int {
-  kVariantBf16N128 = 0,
-  kVariantBf16N256 = 1,
-  kVariantMxN128 = 2,
-  kVariantBf16Pair = 3,
-  kVariantMxPair = 4,
-  kNumVariants = 5
+// Kernel variants: kernel kind (operand format x CTA tile) x operand layout.  The pair kinds
+// run 2-CTA clusters on 256 x 256 tiles (one CTA per 128 rows); `Launch::grid` always counts
+// CTAs.  Layout bit 0: A stored transposed (K x M); bit 1: B stored transposed (N x K); the
+// transposed layouts exist for bf16 only.
+enum Kind : int {
+  kKindBf16N128 = 0,
+  kKindBf16N256 = 1,
+  kKindMxN128 = 2,
+  kKindBf16Pair = 3,
+  kKindMxPair = 4,
+  kNumKinds = 5
 };
-
-inline bool variant_is_pair(int v) { return v == kVariantBf16Pair || v == kVariantMxPair; }
+constexpr int kNumLayouts = 4;
+constexpr int kNumVariants = kNumKinds * kNumLayouts;
+constexpr int variant_of(int kind, int layout) { return kind * kNumLayouts + layout; }
+inline int variant_kind(int v) { return v / kNumLayouts; }
+inline int variant_layout(int v) { return v % kNumLayouts; }
+inline bool variant_is_pair(int v) {
+  return variant_kind(v) == kKindBf16Pair || variant_kind(v) == kKindMxPair;
+}
+// the plain (untransposed) layout of each kind
+enum : int {
+  kVariantBf16N128 = variant_of(kKindBf16N128, 0),
+  kVariantBf16N256 = variant_of(kKindBf16N256, 0),
+  kVariantMxN128 = variant_of(kKindMxN128, 0),
+  kVariantBf16Pair = variant_of(kKindBf16Pair, 0),
+  kVariantMxPair = variant_of(kKindMxPair, 0)
+};
 
 struct Launch {
   const CUtensorMap* tmA;
@@ -31,6 +47,16 @@ struct Launch {
   bool cooperative;   // ask the driver to guarantee that every CTA is resident at once
   cudaStream_t stream;
 };
+
+// Per translation unit: set-up (shared-memory limit + occupancy) and launch of one kind.
+cudaError_t setup_bf16_n128(int layout, int* ctas_per_sm);
+cudaError_t launch_bf16_n128(int layout, const Launch& l);
+cudaError_t setup_bf16_n256(int layout, int* ctas_per_sm);
+cudaError_t launch_bf16_n256(int layout, const Launch& l);
+cudaError_t setup_bf16_pair(int layout, int* max_clusters);
+cudaError_t launch_bf16_pair(int layout, const Launch& l);
+cudaError_t setup_mx_pair(int* max_clusters);
+cudaError_t launch_mx_pair(const Launch& l);
 
 // Dynamic shared memory of a variant, in bytes.
 size_t variant_smem_bytes(int variant);
@@ -51,5 +77,11 @@ size_t pair_variant_smem_bytes(int variant);
 cudaError_t mx_scale_prep(const uint8_t* a_scales, int64_t a_rows, int64_t a_row_blocks,
                           const uint8_t* b_scales, int64_t b_rows, int64_t b_row_blocks,
                           int64_t kblocks, int64_t kgroups, uint8_t* out, cudaStream_t stream);
+
+// Column sums of a row-major M x N bf16 matrix (N even) into N values of fp32 (out_bf16 = 0)
+// or bf16; `scratch` holds colsum_scratch_bytes(M, N) bytes.
+int64_t colsum_scratch_bytes(int64_t M, int64_t N);
+cudaError_t colsum_bf16(const void* x, int64_t M, int64_t N, void* out, int out_bf16,
+                        float* scratch, cudaStream_t stream);
 
 }  // namespace sk

@@ -197,6 +197,17 @@ def test_pair_streamk_wait_that_runs_out_reports_timeout():
     gu.assert_close(gu.host_values(c), ref, "bf16")
 
 
+def test_device_caps_write_only_their_structure():
+    # the structure sits between canary bytes; the call must leave them untouched
+    import ctypes
+    size = ctypes.sizeof(sk.DeviceCaps)
+    buf = (ctypes.c_uint8 * (size + 256))()
+    ctypes.memset(buf, 0xA5, size + 256)
+    st = sk.lib().sk_device_caps(0, ctypes.cast(ctypes.byref(buf, 0), ctypes.POINTER(sk.DeviceCaps)))
+    assert st == sk.SK_OK
+    assert bytes(buf[size:]) == b"\xa5" * 256
+
+
 def test_device_caps_report_the_pair_capacity():
     caps = sk.sk_device_caps(0)
     assert caps["cc"] == (10, 3)

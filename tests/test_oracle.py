@@ -452,3 +452,56 @@ def test_schedule_invariance_of_the_result(mode, g):
     plain = oracle.addmm_bf16(q["A"], q["B"], q["bias"])
     sched = oracle.addmm_bf16_scheduled(q["A"], q["B"], q["bias"], mode, 16, 16, 8, g)
     assert np.allclose(sched, plain, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------------------
+# stored-transposed GEMM and addmm backward
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("ta", [False, True])
+@pytest.mark.parametrize("tb", [False, True])
+def test_transposed_gemm_bruteforce_exact_rationals(ta, tb):
+    rng = np.random.default_rng(40 + 2 * ta + tb)
+    M, N, K = 3, 5, 4
+    A = _dyadic_bf16(rng, (K, M) if ta else (M, K))
+    B = _dyadic_bf16(rng, (N, K) if tb else (K, N))
+    got = oracle.gemm_bf16_t(A, ta, B, tb)
+    for m in range(M):
+        for n in range(N):
+            exact = Fraction(0)
+            for k in range(K):
+                a = A[k, m] if ta else A[m, k]
+                b = B[n, k] if tb else B[k, n]
+                exact += Fraction(_bf16_to_float(int(a))) * Fraction(_bf16_to_float(int(b)))
+            assert Fraction(got[m, n]) == exact
+    ms, ns = np.array([0, 2, 1]), np.array([4, 0, 3])
+    assert np.array_equal(oracle.gemm_bf16_t_at(A, ta, B, tb, ms, ns), got[ms, ns])
+
+
+def test_addmm_backward_matches_torch_autograd_float64():
+    p = inputs.bf16_problem(48, 40, 56, seed=17, bias="f32_normal")
+    dC = inputs.to_bf16_bits(np.random.default_rng(18).standard_normal((48, 40)).astype(np.float32))
+    A = torch.from_numpy(inputs.bf16_bits_to_f32(p["A"]).astype(np.float64)).requires_grad_()
+    B = torch.from_numpy(inputs.bf16_bits_to_f32(p["B"]).astype(np.float64)).requires_grad_()
+    bias = torch.from_numpy(p["bias"].astype(np.float64)).requires_grad_()
+    torch.addmm(bias, A, B).backward(torch.from_numpy(inputs.bf16_bits_to_f32(dC).astype(np.float64)))
+    dA, dB, db = oracle.addmm_backward_bf16(dC, p["A"], p["B"])
+    assert np.allclose(dA, A.grad.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dB, B.grad.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(db, bias.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_addmm_backward_integer_closed_forms():
+    rng = np.random.default_rng(19)
+    M, N, K = 9, 7, 5
+    A = rng.integers(-5, 6, (M, K))
+    B = rng.integers(-5, 6, (K, N))
+    dC = rng.integers(-5, 6, (M, N))
+    bits = lambda x: inputs.to_bf16_bits(x.astype(np.float32))
+    dA, dB, db = oracle.addmm_backward_bf16(bits(dC), bits(A), bits(B))
+    assert np.array_equal(dA, (dC @ B.T).astype(np.float64))
+    assert np.array_equal(dB, (A.T @ dC).astype(np.float64))
+    assert np.array_equal(db, dC.sum(axis=0).astype(np.float64))
+    # the backward GEMMs are the forward GEMM of stored-transposed operands
+    assert np.array_equal(dA, oracle.gemm_bf16_t(bits(dC), False, bits(B), True))
+    assert np.array_equal(dB, oracle.gemm_bf16_t(bits(A), True, bits(dC), False))
