@@ -86,6 +86,13 @@ def _lib():
                                                   i32]
             lib.oracle_addmm_backward_bf16.restype = i32
             lib.oracle_addmm_backward_bf16.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, i32]
+            lib.oracle_e4m3_value.restype = d
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_addmm_fp8_rows.restype = i32
+            lib.oracle_addmm_fp8_rows.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i64, vp, i32]
+            lib.oracle_addmm_fp8_at.restype = i32
+            lib.oracle_addmm_fp8_at.argtypes = [vp, vp, vp, i32, i64, i64, i64, vp, vp, i64, vp,
+                                                i32]
             lib.oracle_hardware_threads.restype = i32
             lib.oracle_hardware_threads.argtypes = []
             _handle = lib
@@ -124,6 +131,10 @@ def e2m1_value(code: int) -> float:
 
 def e8m0_value(e: int) -> float:
     return _lib().oracle_e8m0_value(int(e))
+
+
+def e4m3_value(code: int) -> float:
+    return _lib().oracle_e4m3_value(int(code))
 
 
 def round_bf16(x: float) -> int:
@@ -202,6 +213,37 @@ def addmm_mxfp4_at(A, A_scale, B, B_scale, bias, ms, ns, threads=0):
                                       _ptr(out), threads)
     if rc:
         raise ValueError(f"oracle_addmm_mxfp4_at failed ({rc})")
+    return out
+
+
+def addmm_fp8(A, B, bias=None, rows=None, threads=0):
+    """binary64 C for E4M3 A (M,K) and B (K,N) given as uint8 codes."""
+    A, B = _c(A, np.uint8), _c(B, np.uint8)
+    M, K = A.shape
+    K2, N = B.shape
+    assert K == K2
+    bias, bdt = _bias(bias)
+    m0, m1 = rows if rows is not None else (0, M)
+    out = np.empty((m1 - m0, N), dtype=np.float64)
+    rc = _lib().oracle_addmm_fp8_rows(_ptr(A), _ptr(B), _ptr(bias), bdt, M, N, K, m0, m1,
+                                      _ptr(out), threads)
+    if rc:
+        raise ValueError(f"oracle_addmm_fp8_rows failed ({rc})")
+    return out
+
+
+def addmm_fp8_at(A, B, bias, ms, ns, threads=0):
+    """addmm_fp8 at the positions (ms[i], ns[i])."""
+    A, B = _c(A, np.uint8), _c(B, np.uint8)
+    M, K = A.shape
+    N = B.shape[1]
+    bias, bdt = _bias(bias)
+    ms, ns = _c(ms, np.int64), _c(ns, np.int64)
+    out = np.empty(ms.shape, dtype=np.float64)
+    rc = _lib().oracle_addmm_fp8_at(_ptr(A), _ptr(B), _ptr(bias), bdt, M, N, K, _ptr(ms),
+                                    _ptr(ns), ms.size, _ptr(out), threads)
+    if rc:
+        raise ValueError(f"oracle_addmm_fp8_at failed ({rc})")
     return out
 
 

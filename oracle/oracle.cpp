@@ -70,6 +70,18 @@ double e2m1_value(uint8_t code) {
   return sign ? -magnitude : magnitude;
 }
 
+// OCP FP8 E4M3: bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0 mantissa; exponent 0 is
+// subnormal (m * 2^-9); S.1111.111 is NaN; there are no infinities (largest finite 448).
+double e4m3_value(uint8_t code) {
+  const int sign = (code >> 7) & 1;
+  const int expo = (code >> 3) & 15;
+  const int mant = code & 7;
+  if (expo == 15 && mant == 7) return std::nan("");
+  const double magnitude =
+      expo == 0 ? std::ldexp(static_cast<double>(mant), -9) : std::ldexp(1.0 + mant / 8.0, expo - 7);
+  return sign ? -magnitude : magnitude;
+}
+
 // OCP MX E8M0: 2^(E-127); E = 255 encodes NaN.
 double e8m0_value(uint8_t e) {
   if (e == 255) return std::nan("");
@@ -209,6 +221,7 @@ extern "C" {
 double oracle_bf16_value(uint16_t bits) { return bf16_value(bits); }
 double oracle_e2m1_value(uint8_t code) { return e2m1_value(code); }
 double oracle_e8m0_value(uint8_t e) { return e8m0_value(e); }
+double oracle_e4m3_value(uint8_t code) { return e4m3_value(code); }
 uint16_t oracle_round_bf16(double x) { return round_to_bf16(x); }
 
 // Round n binary64 values to the output type: out_dtype 0 = fp32 (float*), 1 = bf16 (uint16_t*).
@@ -336,6 +349,43 @@ int oracle_addmm_backward_bf16(const uint16_t* dC, const uint16_t* A, const uint
       dbias[n] = s;
     }
   }
+  return 0;
+}
+
+// ---- fp8 (E4M3) addmm -----------------------------------------------------------------------
+// A: M x K bytes, B: K x N bytes, both E4M3, row-major.  Output as for the bf16 form.
+int oracle_addmm_fp8_rows(const uint8_t* A, const uint8_t* B, const void* bias, int bias_dtype,
+                          int64_t M, int64_t N, int64_t K, int64_t m0, int64_t m1, double* out,
+                          int threads) {
+  if (M < 0 || N < 0 || K < 0 || m0 < 0 || m1 > M || m0 > m1) return 1;
+  std::vector<double> Bv(static_cast<size_t>(K * N));
+  for (int64_t i = 0; i < K * N; ++i) Bv[i] = e4m3_value(B[i]);
+  parallel_rows(m0, m1, threads, [&](int64_t m) {
+    double* row = out + (m - m0) * N;
+    for (int64_t n = 0; n < N; ++n) row[n] = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      const double a = e4m3_value(A[m * K + k]);
+      const double* brow = Bv.data() + k * N;
+      for (int64_t n = 0; n < N; ++n) row[n] = row[n] + a * brow[n];
+    }
+    for (int64_t n = 0; n < N; ++n) row[n] = row[n] + bias_value(bias, bias_dtype, n);
+  });
+  return 0;
+}
+
+int oracle_addmm_fp8_at(const uint8_t* A, const uint8_t* B, const void* bias, int bias_dtype,
+                        int64_t M, int64_t N, int64_t K, const int64_t* ms, const int64_t* ns,
+                        int64_t count, double* out, int threads) {
+  for (int64_t i = 0; i < count; ++i)
+    if (ms[i] < 0 || ms[i] >= M || ns[i] < 0 || ns[i] >= N) return 1;
+  double value[256];
+  for (int c = 0; c < 256; ++c) value[c] = e4m3_value(static_cast<uint8_t>(c));
+  parallel_rows(0, count, threads, [&](int64_t i) {
+    const int64_t m = ms[i], n = ns[i];
+    double s = 0.0;
+    for (int64_t k = 0; k < K; ++k) s = s + value[A[m * K + k]] * value[B[k * N + n]];
+    out[i] = s + bias_value(bias, bias_dtype, n);
+  });
   return 0;
 }
 

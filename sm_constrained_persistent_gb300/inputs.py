@@ -8,6 +8,7 @@ Storage conventions (host, numpy):
   * bf16 tensors are ``uint16`` arrays of bf16 bit patterns (rounded from fp32 by torch's
     round-to-nearest-even conversion);
   * fp32 tensors are ``float32``;
+  * fp8 operands are ``uint8`` OCP E4M3 codes (torch ``float8_e4m3fn`` bit patterns);
   * MXFP4 operands are ``uint8`` code bytes, two E2M1 codes per byte packed along K with the
     even-k element in the low nibble, rows x K/2; their E8M0 scales are ``uint8`` rows x K/32.
 
@@ -37,6 +38,35 @@ def _normal_f32(rng, shape, scale):
     if scale != 1.0:
         x *= np.float32(scale)
     return x
+
+
+def to_e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """fp32 array -> OCP FP8 E4M3 codes (uint8), via torch's float8_e4m3fn conversion."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy().copy()
+
+
+def fp8_problem(M, N, K, *, seed, operand_scale="unit", bias="none", integer=False):
+    """E4M3 A (M,K) and B (K,N) codes plus an optional bias (as bf16_problem's).  A is N(0,1);
+    B is N(0,1), or N(0,1)/sqrt(K) for operand_scale "sqrt_k", so that C stays O(1)."""
+    rng = np.random.default_rng(seed)
+    if integer:
+        A = to_e4m3_codes(rng.integers(-8, 9, size=(M, K)).astype(np.float32))
+        B = to_e4m3_codes(rng.integers(-8, 9, size=(K, N)).astype(np.float32))
+    else:
+        s = 1.0 if operand_scale == "unit" else 1.0 / np.sqrt(K)
+        A = to_e4m3_codes(_normal_f32(rng, (M, K), 1.0))
+        B = to_e4m3_codes(_normal_f32(rng, (K, N), s))
+    b = None
+    if bias == "f32_normal":
+        b = rng.standard_normal(size=N, dtype=np.float32)
+    elif bias == "bf16_uniform":
+        b = to_bf16_bits(rng.uniform(-1.0, 1.0, size=N).astype(np.float32))
+    elif bias == "f32_int":
+        b = rng.integers(-8, 9, size=N).astype(np.float32)
+    elif bias != "none":
+        raise ValueError(bias)
+    return {"A": A, "B": B, "bias": b, "M": M, "N": N, "K": K}
 
 
 def bf16_problem(M, N, K, *, seed, operand_scale="unit", bias="none", integer=False):
@@ -118,6 +148,8 @@ WORKLOADS = {
                        dict(operand_scale="sqrt_k", bias="none"), "bf16", 1238),
     "gemm_bf16_skinny_64x14336x4096": ("bf16", 64, 14336, 4096,
                                        dict(operand_scale="sqrt_k", bias="none"), "bf16", 1238),
+    "addmm_fp8_8192": ("fp8", 8192, 8192, 8192,
+                       dict(operand_scale="sqrt_k", bias="bf16_uniform"), "bf16", 1239),
 }
 
 
@@ -126,6 +158,8 @@ def workload(name, seed=None):
     s = default_seed if seed is None else seed
     if fmt == "bf16":
         p = bf16_problem(M, N, K, seed=s, **kw)
+    elif fmt == "fp8":
+        p = fp8_problem(M, N, K, seed=s, **kw)
     else:
         p = mxfp4_problem(M, N, K, seed=s, **kw)
     p["format"], p["out_dtype"] = fmt, out

@@ -505,3 +505,60 @@ def test_addmm_backward_integer_closed_forms():
     # the backward GEMMs are the forward GEMM of stored-transposed operands
     assert np.array_equal(dA, oracle.gemm_bf16_t(bits(dC), False, bits(B), True))
     assert np.array_equal(dB, oracle.gemm_bf16_t(bits(A), True, bits(dC), False))
+
+
+# ---------------------------------------------------------------------------------------
+# fp8 (E4M3)
+# ---------------------------------------------------------------------------------------
+
+def test_e4m3_decode_matches_torch_float8_and_the_format_limits():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        v = oracle.e4m3_value(c)
+        if math.isnan(ref[c]):
+            assert math.isnan(v), c
+        else:
+            assert v == ref[c] and math.copysign(1, v) == math.copysign(1, ref[c]), c
+    assert oracle.e4m3_value(0x7E) == 448.0            # largest finite
+    assert oracle.e4m3_value(0x01) == 2.0 ** -9         # smallest subnormal
+    assert oracle.e4m3_value(0x08) == 2.0 ** -6         # smallest normal
+    assert oracle.e4m3_value(0x38) == 1.0 and oracle.e4m3_value(0xC4) == -3.0
+    assert math.isnan(oracle.e4m3_value(0x7F)) and math.isnan(oracle.e4m3_value(0xFF))
+
+
+def test_fp8_bruteforce_exact_rationals_and_cross_format():
+    rng = np.random.default_rng(61)
+    M, N, K = 4, 6, 9
+    A = rng.integers(0, 256, (M, K)).astype(np.uint8)
+    B = rng.integers(0, 256, (K, N)).astype(np.uint8)
+    A[(A & 0x7F) == 0x7F] = 0x3C          # no NaN codes
+    B[(B & 0x7F) == 0x7F] = 0x44
+    bias = rng.standard_normal(N).astype(np.float32)
+    got = oracle.addmm_fp8(A, B, bias)
+
+    def dec(c):      # sign, exponent and mantissa fields read by hand, as exact rationals
+        c = int(c)
+        e, m = (c >> 3) & 15, c & 7
+        v = Fraction(m, 512) if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+        return -v if c & 0x80 else v
+
+    for m in range(M):
+        for n in range(N):
+            exact = sum(dec(A[m, k]) * dec(B[k, n]) for k in range(K)) + Fraction(float(bias[n]))
+            assert Fraction(got[m, n]) == exact
+    # decoded E4M3 values are exact in bf16: the fp8 GEMM equals the bf16 GEMM of them
+    a16 = inputs.to_bf16_bits(torch.from_numpy(A).view(torch.float8_e4m3fn).float().numpy())
+    b16 = inputs.to_bf16_bits(torch.from_numpy(B).view(torch.float8_e4m3fn).float().numpy())
+    assert np.array_equal(got, oracle.addmm_bf16(a16, b16, bias))
+    ms, ns = np.array([0, 3, 2]), np.array([5, 1, 0])
+    assert np.array_equal(oracle.addmm_fp8_at(A, B, bias, ms, ns), got[ms, ns])
+    assert np.array_equal(oracle.addmm_fp8(A, B, bias, rows=(1, 3)), got[1:3])
+
+
+def test_fp8_generator_draws_exact_integers_and_no_nan():
+    p = inputs.fp8_problem(64, 48, 96, seed=2, integer=True, bias="f32_int")
+    vals = torch.from_numpy(p["A"]).view(torch.float8_e4m3fn).float().numpy()
+    assert np.all(vals == np.round(vals)) and np.abs(vals).max() <= 8
+    q = inputs.fp8_problem(64, 48, 96, seed=2, operand_scale="sqrt_k")
+    assert not np.any((q["A"] & 0x7F) == 0x7F) and not np.any((q["B"] & 0x7F) == 0x7F)
