@@ -33,6 +33,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # fp4 dense peak relative to bf16 dense (nominal 13.5 / 2.25 PFLOP/s; MXFP4 with E8M0 scales
 # runs at the fp4 rate)
 FP4_OVER_BF16 = 13.5 / 2.25
+# fp8 dense peak relative to bf16 dense (nominal 4.5 / 2.25 PFLOP/s)
+FP8_OVER_BF16 = 4.5 / 2.25
+FORMAT_CODE = {"bf16": 0, "mxfp4": 1, "fp8": 2}
+DTYPE_NAME = {"bf16": "bf16", "mxfp4": "mxfp4(e2m1+e8m0)", "fp8": "fp8(e4m3)"}
 
 
 def parse_args(argv=None):
@@ -228,6 +232,8 @@ class Problem:
         if self.fmt == "bf16":
             self.host = {"A": pinned(p["A"].view(np.int16), torch.bfloat16),
                          "B": pinned(p["B"].view(np.int16), torch.bfloat16)}
+        elif self.fmt == "fp8":
+            self.host = {"A": pinned(p["A"]), "B": pinned(p["B"])}
         else:
             self.host = {"A": pinned(p["A"]), "A_scale": pinned(p["A_scale"]),
                          "B": pinned(p["B"]), "B_scale": pinned(p["B_scale"])}
@@ -262,6 +268,14 @@ class Problem:
             return sk.sk_gemm_bf16_ex(d["A"].data_ptr(), d["B"].data_ptr(), bias,
                                       self.C.data_ptr(), od, self.M, self.N, self.K, num_sms, m,
                                       options, stream_ptr)
+        if self.fmt == "fp8":
+            if options is None:
+                return sk.sk_gemm_fp8(d["A"].data_ptr(), d["B"].data_ptr(), bias,
+                                      self.C.data_ptr(), od, self.M, self.N, self.K, num_sms, m,
+                                      stream_ptr)
+            return sk.sk_gemm_fp8_ex(d["A"].data_ptr(), d["B"].data_ptr(), bias,
+                                     self.C.data_ptr(), od, self.M, self.N, self.K, num_sms, m,
+                                     options, stream_ptr)
         if options is None:
             return sk.sk_gemm_mxfp4(d["A"].data_ptr(), d["A_scale"].data_ptr(), d["B"].data_ptr(),
                                     d["B_scale"].data_ptr(), bias, self.C.data_ptr(), od, self.M,
@@ -271,7 +285,7 @@ class Problem:
                                    self.N, self.K, num_sms, m, options, stream_ptr)
 
     def kernels_per_call(self):
-        return 1 if self.fmt == "bf16" else 3   # MXFP4: two scale-layout kernels + the GEMM
+        return 2 if self.fmt == "mxfp4" else 1   # MXFP4: the scale-layout kernel + the GEMM
 
 
 L2_FLUSH_BYTES = 256 << 20   # twice the 129 MB L2
@@ -357,6 +371,8 @@ def cpu_baseline(prob, seconds):
         t0 = time.perf_counter()
         if prob.fmt == "bf16":
             oracle.addmm_bf16(p["A"], p["B"], p["bias"], rows=(0, rows), threads=threads)
+        elif prob.fmt == "fp8":
+            oracle.addmm_fp8(p["A"], p["B"], p["bias"], rows=(0, rows), threads=threads)
         else:
             oracle.addmm_mxfp4(p["A"], p["A_scale"], p["B"], p["B_scale"], p["bias"],
                                rows=(0, rows), threads=threads)
@@ -395,18 +411,21 @@ def run_ours(args):
     value = flops_all / (ms_max * args.steps * 1e-3) / 1e12
     clock = clocks.summary()
 
-    plan = sk.sk_plan(0 if prob.fmt == "bf16" else 1, prob.M, prob.N, prob.K, args.num_sms,
+    plan = sk.sk_plan(FORMAT_CODE[prob.fmt], prob.M, prob.N, prob.K, args.num_sms,
                       args.mode, sm_count)
     peaks, peak_src = measured_peaks()
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     if prob.fmt == "bf16":
         peak, peak_note = bf16_peak, f"bf16 dense, burst, {peak_src}"
+    elif prob.fmt == "fp8":
+        peak = bf16_peak * FP8_OVER_BF16
+        peak_note = f"fp8 dense = {peak_src} bf16 burst x {FP8_OVER_BF16:g} (nominal ratio)"
     else:
         peak = bf16_peak * FP4_OVER_BF16
         peak_note = f"fp4 dense = {peak_src} bf16 burst x {FP4_OVER_BF16:g} (nominal ratio)"
     gemm_ms = statistics.mean(per)   # one GEMM kernel dominates each call
     achieved = prob.flops / (gemm_ms * 1e-3) / 1e12
-    kernel_key = (f"gemm<{'mxfp4' if prob.fmt != 'bf16' else 'bf16'},{plan.tile_m}x{plan.tile_n}>"
+    kernel_key = (f"gemm<{prob.fmt},{plan.tile_m}x{plan.tile_n}>"
                   f":{args.workload}:{args.mode}")
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
@@ -425,7 +444,7 @@ def run_ours(args):
         "metric": HEADLINE_METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if prob.fmt == "bf16" else "mxfp4(e2m1+e8m0)", "data": "synthetic",
+        "dtype": DTYPE_NAME[prob.fmt], "data": "synthetic",
         "config": {"workload": args.workload, "M": prob.M, "N": prob.N, "K": prob.K,
                    "format": prob.fmt, "out": str(prob.out_dtype).replace("torch.", ""),
                    "bias": prob.p["bias"] is not None, "mode": args.mode,
@@ -458,7 +477,7 @@ def _time_modes(pr, modes, sm_count, peak, dist, num_sms=0, options=None, steps=
     for mode in modes:
         total, _ = time_calls(pr, mode, num_sms, steps, warmup, dist, options)
         ms = total / steps
-        plan = sk.sk_plan(0 if pr.fmt == "bf16" else 1, pr.M, pr.N, pr.K, num_sms, mode, sm_count,
+        plan = sk.sk_plan(FORMAT_CODE[pr.fmt], pr.M, pr.N, pr.K, num_sms, mode, sm_count,
                           options)
         tflops = pr.flops / (ms * 1e-3) / 1e12
         res[mode] = {"ms": round(ms, 4), "tflops": round(tflops, 1),
@@ -578,9 +597,9 @@ def extras(prob, sm_count, dist):
             cache[name] = Problem(name, prob.device)
         return cache[name]
 
-    for name in ["addmm_bf16_8192", "addmm_mxfp4_8192"]:
+    for name in ["addmm_bf16_8192", "addmm_mxfp4_8192", "addmm_fp8_8192"]:
         pr = get(name)
-        peak = bpeak if pr.fmt == "bf16" else bpeak * FP4_OVER_BF16
+        peak = bpeak * {"bf16": 1.0, "mxfp4": FP4_OVER_BF16, "fp8": FP8_OVER_BF16}[pr.fmt]
         out[name] = _time_modes(pr, modes, sm_count, peak, dist)
     # the wave-quantised shape: its stated 128x128 tiles (225 tiles) and the automatic choice
     pr = get("gemm_bf16_1920x1920x16384")
@@ -632,6 +651,8 @@ def run_reference(args):
     def step():
         if p["format"] == "bf16":
             oracle.addmm_bf16(p["A"], p["B"], p["bias"], rows=(0, rows), threads=threads)
+        elif p["format"] == "fp8":
+            oracle.addmm_fp8(p["A"], p["B"], p["bias"], rows=(0, rows), threads=threads)
         else:
             oracle.addmm_mxfp4(p["A"], p["A_scale"], p["B"], p["B_scale"], p["bias"],
                                rows=(0, rows), threads=threads)

@@ -143,6 +143,24 @@ sk_status_t sk_gemm_mxfp4_ex(const void* A, const void* A_scale, const void* B,
                              sk_mode_t mode, const sk_options_t* options, void* stream);
 
 /*
+ * sk_gemm_fp8 / sk_gemm_fp8_ex — the same product for 8-bit float operands (OCP FP8 E4M3: 1 sign
+ * bit, 4 exponent bits with bias 7, 3 mantissa bits, largest finite 448, S.1111.111 = NaN, no
+ * infinities), as taken by the SM-constraint GEMM of flashinfer PR #982 ("float8_e4m3fn",
+ * review comments on the 16-byte minimum chunk).  Products accumulate in fp32.
+ *   A: M x K bytes row-major; B: K x N bytes row-major (the torch `mm(a, b)` layout).
+ *   K and N must be multiples of 16 (16-byte row pitches).  bias, C, out_dtype and the
+ *   schedule arguments as sk_gemm_bf16 / sk_gemm_bf16_ex.  No scaling is applied (a per-tensor
+ *   scale, if any, belongs to the caller).  Errors as sk_gemm_bf16.
+ */
+sk_status_t sk_gemm_fp8(const void* A, const void* B, const void* bias, void* C,
+                        sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
+                        sk_mode_t mode, void* stream);
+
+sk_status_t sk_gemm_fp8_ex(const void* A, const void* B, const void* bias, void* C,
+                           sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
+                           sk_mode_t mode, const sk_options_t* options, void* stream);
+
+/*
  * sk_gemm_bf16_t — C[M x N] = op(A) * op(B) (+ bias[N]) with either bf16 operand stored
  * transposed, through the same schedules and kernels (operands read M-major / K-major by the
  * tensor cores, no copy).
@@ -234,7 +252,8 @@ sk_status_t sk_device_caps(int device, sk_device_caps_t* caps);
 
 /*
  * Planning (host only, makes no CUDA call).  Fills *plan with the schedule the library would
- * launch for this problem on a device with `sm_count` SMs.  format: 0 = bf16, 1 = MXFP4.
+ * launch for this problem on a device with `sm_count` SMs.  format: 0 = bf16, 1 = MXFP4,
+ * 2 = fp8 (E4M3).
  */
 typedef struct {
   int32_t format;

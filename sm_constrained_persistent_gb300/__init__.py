@@ -81,6 +81,11 @@ def lib():
             h.sk_gemm_mxfp4_ex.restype = i32
             h.sk_gemm_mxfp4_ex.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, i32, i32,
                                            ctypes.POINTER(Options), vp]
+            h.sk_gemm_fp8.restype = i32
+            h.sk_gemm_fp8.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, i32, vp]
+            h.sk_gemm_fp8_ex.restype = i32
+            h.sk_gemm_fp8_ex.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, i32,
+                                         ctypes.POINTER(Options), vp]
             h.sk_gemm_bf16_t.restype = i32
             h.sk_gemm_bf16_t.argtypes = [vp, i32, vp, i32, vp, vp, i32, i64, i64, i64, i32, i32,
                                          ctypes.POINTER(Options), vp]
@@ -140,6 +145,15 @@ def sk_gemm_mxfp4_ex(A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sm
                      options, stream):
     return lib().sk_gemm_mxfp4_ex(A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sms,
                                   mode, _opts(options), stream)
+
+
+def sk_gemm_fp8(A, B, bias, C, out_dtype, M, N, K, num_sms, mode, stream):
+    return lib().sk_gemm_fp8(A, B, bias, C, out_dtype, M, N, K, num_sms, mode, stream)
+
+
+def sk_gemm_fp8_ex(A, B, bias, C, out_dtype, M, N, K, num_sms, mode, options, stream):
+    return lib().sk_gemm_fp8_ex(A, B, bias, C, out_dtype, M, N, K, num_sms, mode,
+                                _opts(options), stream)
 
 
 def sk_gemm_bf16_t(A, trans_a, B, trans_b, bias, C, out_dtype, M, N, K, num_sms, mode, options,
@@ -265,6 +279,31 @@ def gemm_mxfp4(a, a_scale, b, b_scale, bias=None, out=None, out_dtype=None, num_
                           bias.data_ptr() if bias is not None else None, out.data_ptr(), od,
                           M, N, K, num_sms, _mode(mode), options, _stream_ptr(stream))
     _check(st, "sk_gemm_mxfp4")
+    return out
+
+
+def gemm_fp8(a, b, bias=None, out=None, out_dtype=None, num_sms=0, mode="streamk",
+             options=None, stream=None):
+    """C = a @ b (+ bias) for E4M3 CUDA tensors a (M,K), b (K,N), given as float8_e4m3fn or as
+    uint8 codes; returns C (bf16 or fp32)."""
+    import torch
+    M, K = a.shape
+    N = b.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=a.device)
+    for t in (a, b, out) + ((bias,) if bias is not None else ()):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    ok = (torch.uint8, torch.float8_e4m3fn)
+    if a.dtype not in ok or b.dtype not in ok:
+        raise TypeError("a and b must be float8_e4m3fn (or uint8 codes)")
+    od = SK_BF16 if out.dtype == torch.bfloat16 else SK_F32
+    if bias is not None and bias.dtype != out.dtype:
+        raise TypeError("bias must have the output dtype")
+    st = sk_gemm_fp8_ex(a.data_ptr(), b.data_ptr(), bias.data_ptr() if bias is not None else None,
+                        out.data_ptr(), od, M, N, K, num_sms, _mode(mode), options,
+                        _stream_ptr(stream))
+    _check(st, "sk_gemm_fp8")
     return out
 
 

@@ -19,6 +19,7 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kBf16TileK = 64;
 constexpr int kMxTileK = 256;
+constexpr int kF8TileK = 128;
 constexpr int kDefaultRasterGroup = 16;
 constexpr int64_t kDefaultTimeoutNs = 2000000000LL;   // 2 s
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
@@ -33,7 +34,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // sm_count / 2 when it cannot ask the device).
 sk_status_t make_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, int mode,
                       int sm_count, int max_pairs, const sk_options_t* opt, sk_plan_t* p) {
-  if (p == nullptr || (format != 0 && format != 1) || mode < 0 || mode > 3 || sm_count < 1)
+  if (p == nullptr || format < 0 || format > 2 || mode < 0 || mode > 3 || sm_count < 1)
     return SK_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return SK_ERR_INVALID_ARG;
@@ -77,7 +78,7 @@ sk_status_t make_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, 
   p->mode = mode;
   p->tile_m = tile_m;
   p->tile_n = tile_n;
-  p->tile_k = format == 1 ? kMxTileK : kBf16TileK;
+  p->tile_k = format == 1 ? kMxTileK : (format == 2 ? kF8TileK : kBf16TileK);
   p->ctas_per_tile = pair ? 2 : 1;
   const int64_t tiles_m = ceil_div(M, tile_m), tiles_n = ceil_div(N, tile_n);
   const int64_t tiles = tiles_m * tiles_n;
@@ -315,6 +316,9 @@ sk_status_t validate(int format, const void* A, const void* A_scale, const void*
     const int64_t a_pitch = (layout & 1) ? M : K;
     const int64_t b_pitch = (layout & 2) ? K : N;
     if (a_pitch % 8 != 0 || b_pitch % 8 != 0 || N % 8 != 0) return SK_ERR_INVALID_ARG;
+  } else if (format == 2) {
+    if (layout != 0) return SK_ERR_INVALID_ARG;
+    if (K % 16 != 0 || N % 16 != 0) return SK_ERR_INVALID_ARG;   // 16-byte row pitches
   } else {
     if (layout != 0) return SK_ERR_INVALID_ARG;
     if (A_scale == nullptr || B_scale == nullptr) return SK_ERR_INVALID_ARG;
@@ -348,8 +352,9 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   if (di->cc_major != 10 || di->cc_minor != 3) return SK_ERR_UNSUPPORTED;   // built for sm_103a
 
   // The pair variants' cluster capacity is needed to plan; set both candidates up first.
-  const int pair_variant = format == 1 ? sk::kVariantMxPair
-                                       : sk::variant_of(sk::kKindBf16Pair, layout);
+  const int pair_variant = format == 1   ? sk::kVariantMxPair
+                           : format == 2 ? sk::variant_of(sk::kKindF8Pair, 0)
+                                         : sk::variant_of(sk::kKindBf16Pair, layout);
   if ((st = ensure_variant(*di, pair_variant)) != SK_OK) return st;
   sk_plan_t plan;
   if ((st = make_plan(format, M, N, K, num_sms, mode, di->sm_count, di->max_pairs[pair_variant],
@@ -358,9 +363,10 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   const bool pair = plan.ctas_per_tile == 2;
   const int variant =
       pair ? pair_variant
-           : (format == 1 ? sk::kVariantMxN128
-                          : sk::variant_of(plan.tile_n == 256 ? sk::kKindBf16N256 : sk::kKindBf16N128,
-                                           layout));
+      : format == 1 ? sk::kVariantMxN128
+      : format == 2 ? sk::variant_of(plan.tile_n == 256 ? sk::kKindF8N256 : sk::kKindF8N128, 0)
+                    : sk::variant_of(plan.tile_n == 256 ? sk::kKindBf16N256 : sk::kKindBf16N128,
+                                     layout);
   if ((st = ensure_variant(*di, variant)) != SK_OK) return st;
   const bool streamk = plan.sk_tiles > 0;
   if (streamk) {
@@ -391,6 +397,10 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
                        : encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, M, K, 64, kTileM)) &&
          ((layout & 2) ? encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, 64, bt_rows)
                        : encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, 64, 64));
+  } else if (format == 2) {
+    // fp8 as bytes: A M x K (box 128 k x 128 rows), B K x N (box 128 n x 128 k-rows).
+    ok = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, M, K, 128, kTileM) &&
+         encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, 128, 128);
   } else {
     ok = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, M, K / 2, 128, kTileM) &&
          encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, N, K / 2, 128, b_box);
@@ -471,6 +481,20 @@ sk_status_t sk_gemm_mxfp4_ex(const void* A, const void* A_scale, const void* B,
                              sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
                              sk_mode_t mode, const sk_options_t* options, void* stream) {
   return run_gemm(1, A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sms, mode, options,
+                  stream);
+}
+
+sk_status_t sk_gemm_fp8(const void* A, const void* B, const void* bias, void* C,
+                        sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
+                        sk_mode_t mode, void* stream) {
+  return run_gemm(2, A, nullptr, B, nullptr, bias, C, out_dtype, M, N, K, num_sms, mode, nullptr,
+                  stream);
+}
+
+sk_status_t sk_gemm_fp8_ex(const void* A, const void* B, const void* bias, void* C,
+                           sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
+                           sk_mode_t mode, const sk_options_t* options, void* stream) {
+  return run_gemm(2, A, nullptr, B, nullptr, bias, C, out_dtype, M, N, K, num_sms, mode, options,
                   stream);
 }
 

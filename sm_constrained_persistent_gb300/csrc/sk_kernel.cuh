@@ -53,15 +53,21 @@ enum : uint32_t {
 
 
 // kAT: A is stored transposed (K x M row-major) and read M-major; kBT: B is stored transposed
-// (N x K row-major) and read K-major.  Both are bf16-only.
-template <bool kMx, int kBN, bool kAT = false, bool kBT = false>
+// (N x K row-major) and read K-major.  kF8: 1-byte E4M3 operands instead of bf16 (same layouts).
+template <bool kMx, int kBN, bool kAT = false, bool kBT = false, bool kF8 = false>
 struct Cfg {
   static_assert(kBN == 128 || kBN == 256, "tile width");
-  static_assert(!kMx || (!kAT && !kBT), "MXFP4 operands are K-major");
+  static_assert(!kMx || (!kAT && !kBT && !kF8), "MXFP4 operands are K-major");
   static_assert(!kMx || kBN == 128, "MXFP4 tiles are 128 wide");
-  static constexpr int kTileK = kMx ? 256 : 64;        // K elements per k-iteration (128 B rows)
-  static constexpr int kMmaK = kMx ? 64 : 16;          // K per tcgen05.mma
-  static constexpr int kMmasPerStage = kTileK / kMmaK; // 4
+  // One k-iteration is one 128-byte swizzle row of K: 64 bf16, 128 fp8 or 256 fp4 elements.
+  static constexpr int kTileK = kMx ? 256 : (kF8 ? 128 : 64);
+  static constexpr int kMmaK = kMx ? 64 : (kF8 ? 32 : 16);   // K per tcgen05.mma (32 bytes)
+  static constexpr int kMmasPerStage = kTileK / kMmaK;        // 4
+  // MN-major tiles are blocks of 128 bytes (kAtom elements) x kTileK k-rows, kBoxBytes each;
+  // one MMA's K advances kMnAdvance bytes through a block.
+  static constexpr int kAtom = kF8 ? 128 : 64;
+  static constexpr int kBoxBytes = kTileK * 128;
+  static constexpr int kMnAdvance = kMmaK * 128;
   static constexpr int kStageA = kBM * 128;
   static constexpr int kStageB = kBN * 128;
   static constexpr int kStageSfa = kMx ? 1024 : 0;               // 2 k groups x 512 B
@@ -84,8 +90,9 @@ struct Cfg {
   static constexpr uint32_t kIdesc =
       kMx ? ((1u << 7) | (1u << 10) | (1u << 23) | (uint32_t(kBN >> 3) << 17) |
              (uint32_t(kBM >> 4) << 24))
-          : ((1u << 4) | (1u << 7) | (1u << 10) | (kAT ? (1u << 15) : 0u) |
+          : ((1u << 4) | (kF8 ? 0u : ((1u << 7) | (1u << 10))) | (kAT ? (1u << 15) : 0u) |
              (kBT ? 0u : (1u << 16)) | (uint32_t(kBN >> 3) << 17) | (uint32_t(kBM >> 4) << 24));
+  // (A/B format fields: bf16 = 1 for kind::f16, E4M3 = 0 for kind::f8f6f4)
 };
 
 __device__ __forceinline__ void record_error(const Args& a, uint32_t site, int64_t tile) {
@@ -208,11 +215,11 @@ __device__ __forceinline__ void store_row_chunk(const Args& a, int64_t m, int64_
   }
 }
 
-template <bool kMx, int kBN, bool kAT = false, bool kBT = false>
+template <bool kMx, int kBN, bool kAT = false, bool kBT = false, bool kF8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ Args args) {
-  using Cf = Cfg<kMx, kBN, kAT, kBT>;
+  using Cf = Cfg<kMx, kBN, kAT, kBT, kF8>;
   constexpr int S = Cf::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -296,20 +303,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         args.sfb + (nb * args.sf_kgroups + 2 * k) * 512, 1024, &full[stage]);
             }
           } else {
-            // A: K-major tile (rows x 64 k), or M-major (64 k-rows x 128 m, two 64-wide boxes).
+            constexpr int TK = Cf::kTileK, AT = Cf::kAtom, BX = Cf::kBoxBytes;
+            // A: K-major tile (128 rows x TK), or M-major (TK k-rows x 128 m, AT-wide boxes).
             if constexpr (kAT) {
-              tma_load_2d(sa, &tmA, &full[stage], tm * kBM, k * 64);
-              tma_load_2d(sa + 8192, &tmA, &full[stage], tm * kBM + 64, k * 64);
+#pragma unroll
+              for (int j = 0; j < kBM / AT; ++j)
+                tma_load_2d(sa + j * BX, &tmA, &full[stage], tm * kBM + j * AT, k * TK);
             } else {
-              tma_load_2d(sa, &tmA, &full[stage], k * 64, tm * kBM);
+              tma_load_2d(sa, &tmA, &full[stage], k * TK, tm * kBM);
             }
-            // B: MN-major (64 k-rows x BN n, 64-wide boxes), or K-major (BN rows x 64 k).
+            // B: MN-major (TK k-rows x BN n, AT-wide boxes), or K-major (BN rows x TK k).
             if constexpr (kBT) {
-              tma_load_2d(sb, &tmB, &full[stage], k * 64, tn * kBN);
+              tma_load_2d(sb, &tmB, &full[stage], k * TK, tn * kBN);
             } else {
 #pragma unroll
-              for (int j = 0; j < kBN / 64; ++j)
-                tma_load_2d(sb + j * 8192, &tmB, &full[stage], tn * kBN + j * 64, k * 64);
+              for (int j = 0; j < kBN / AT; ++j)
+                tma_load_2d(sb + j * BX, &tmB, &full[stage], tn * kBN + j * AT, k * TK);
             }
           }
           ++issued;
@@ -387,12 +396,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; K advances 32 B.
               // B: MN-major, 128-byte swizzle; 64-column blocks 8 KB apart (leading offset),
               //    8-row K groups 1024 B apart (stride offset); K advances 16 rows = 2 KB.
-              // M-major A / MN-major B: 64-wide blocks 8 KB apart, K advances 16 rows = 2 KB.
-              const uint64_t ad = kAT ? smem_desc(a0 + j * 2048, 8192, 1024, kLayoutSwizzle128B)
+              // K-major: K advances 32 bytes along the swizzled row.  M-major A / MN-major B:
+              // blocks of 128-byte rows kBoxBytes apart, K advances kMmaK rows.
+              constexpr uint32_t BX = Cf::kBoxBytes, ADV = Cf::kMnAdvance;
+              const uint64_t ad = kAT ? smem_desc(a0 + j * ADV, BX, 1024, kLayoutSwizzle128B)
                                       : smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
               const uint64_t bd = kBT ? smem_desc(b0 + j * 32, 16, 1024, kLayoutSwizzle128B)
-                                      : smem_desc(b0 + j * 2048, 8192, 1024, kLayoutSwizzle128B);
-              mma_f16(d_tmem, ad, bd, Cf::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
+                                      : smem_desc(b0 + j * ADV, BX, 1024, kLayoutSwizzle128B);
+              if constexpr (kF8) {
+                mma_f8(d_tmem, ad, bd, Cf::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
+              } else {
+                mma_f16(d_tmem, ad, bd, Cf::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
+              }
             }
           }
           mma_commit(&empty[stage]);

@@ -52,6 +52,9 @@ size_t variant_smem_bytes(int variant) {
     case kKindBf16N256: return Cfg<false, 256>::kSmemBytes;
     case kKindMxN128: return Cfg<true, 128>::kSmemBytes;
     case kKindBf16Pair: return PairCfg<false>::kSmemBytes;
+    case kKindF8N128: return Cfg<false, 128, false, false, true>::kSmemBytes;
+    case kKindF8N256: return Cfg<false, 256, false, false, true>::kSmemBytes;
+    case kKindF8Pair: return PairCfg<false, false, false, true>::kSmemBytes;
     default: return PairCfg<true>::kSmemBytes;
   }
 }
@@ -70,6 +73,8 @@ cudaError_t variant_setup(int variant, int* ctas_per_sm) {
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gemm_kernel<true, 128>,
                                                            kThreads, Cf::kSmemBytes);
     }
+    case kKindF8N128:
+    case kKindF8N256: return setup_f8(variant_kind(variant), ctas_per_sm);
     default: return cudaErrorInvalidValue;   // pair kinds: pair_variant_setup
   }
 }
@@ -93,16 +98,20 @@ cudaError_t variant_launch(int variant, const Launch& l) {
       cfg.numAttrs = 1;
       return cudaLaunchKernelEx(&cfg, gemm_kernel<true, 128>, *l.tmA, *l.tmB, l.args);
     }
+    case kKindF8N128:
+    case kKindF8N256: return launch_f8(variant_kind(variant), l);
     default: return cudaErrorInvalidValue;   // pair kinds: pair_variant_launch
   }
 }
 
 cudaError_t pair_variant_setup(int variant, int* max_clusters) {
+  if (variant_kind(variant) == kKindF8Pair) return setup_f8(kKindF8Pair, max_clusters);
   return variant_kind(variant) == kKindMxPair ? setup_mx_pair(max_clusters)
                                               : setup_bf16_pair(variant_layout(variant), max_clusters);
 }
 
 cudaError_t pair_variant_launch(int variant, const Launch& l) {
+  if (variant_kind(variant) == kKindF8Pair) return launch_f8(kKindF8Pair, l);
   return variant_kind(variant) == kKindMxPair ? launch_mx_pair(l)
                                               : launch_bf16_pair(variant_layout(variant), l);
 }

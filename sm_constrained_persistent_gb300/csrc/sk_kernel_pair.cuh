@@ -82,6 +82,16 @@ __device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, u
       : "memory");
 }
 
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                               uint32_t idesc, uint32_t sfa_tmem,
                                               uint32_t sfb_tmem, uint32_t accumulate) {
@@ -127,14 +137,17 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-template <bool kMx, bool kAT = false, bool kBT = false>
+template <bool kMx, bool kAT = false, bool kBT = false, bool kF8 = false>
 struct PairCfg {
-  static_assert(!kMx || (!kAT && !kBT), "MXFP4 operands are K-major");
+  static_assert(!kMx || (!kAT && !kBT && !kF8), "MXFP4 operands are K-major");
   static constexpr int kBN = 256;                        // pair tile: 256 x 256
   static constexpr int kHalfN = kBN / 2;                 // B columns loaded by each CTA
-  static constexpr int kTileK = kMx ? 256 : 64;
-  static constexpr int kMmaK = kMx ? 64 : 16;
+  static constexpr int kTileK = kMx ? 256 : (kF8 ? 128 : 64);   // one 128-byte row of K
+  static constexpr int kMmaK = kMx ? 64 : (kF8 ? 32 : 16);
   static constexpr int kMmasPerStage = kTileK / kMmaK;   // 4
+  static constexpr int kAtom = kF8 ? 128 : 64;           // MN-major block width (128 bytes)
+  static constexpr int kBoxBytes = kTileK * 128;
+  static constexpr int kMnAdvance = kMmaK * 128;
   static constexpr int kStageA = kBM * 128;              // 16 KB
   static constexpr int kStageB = kHalfN * 128;           // 16 KB
   static constexpr int kStageSfa = kMx ? 1024 : 0;       // own 128 rows, 2 k groups
@@ -156,18 +169,18 @@ struct PairCfg {
   static constexpr uint32_t kIdesc =
       kMx ? ((1u << 7) | (1u << 10) | (1u << 23) | (uint32_t(kBN >> 3) << 17) |
              (uint32_t(256 >> 4) << 24))
-          : ((1u << 4) | (1u << 7) | (1u << 10) | (kAT ? (1u << 15) : 0u) |
+          : ((1u << 4) | (kF8 ? 0u : ((1u << 7) | (1u << 10))) | (kAT ? (1u << 15) : 0u) |
              (kBT ? 0u : (1u << 16)) | (uint32_t(kBN >> 3) << 17) | (uint32_t(256 >> 4) << 24));
 };
 
 // Registers are granted per 128-thread warpgroup, so 320 or 352 threads are charged as 384:
 // the launch bound caps the kernel at 65536 / 384 -> 168 registers per thread.
-template <bool kMx, bool kAT = false, bool kBT = false>
+template <bool kMx, bool kAT = false, bool kBT = false, bool kF8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSfa,
                      const __grid_constant__ CUtensorMap tmSfb, const __grid_constant__ Args args) {
-  using Cf = PairCfg<kMx, kAT, kBT>;
+  using Cf = PairCfg<kMx, kAT, kBT, kF8>;
   constexpr int S = Cf::kStages;
   constexpr int kBN = Cf::kBN;
   extern __shared__ uint8_t smem_raw[];
@@ -267,17 +280,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
             tma_load_2d_pair(ring_sfb + stage * Cf::kStageSfb + 1024, &tmSfb, fb, 0,
                              (tn * 2 + 1) * plan.iters + k);
           } else {
-            if constexpr (kAT) {   // M-major A: two 64-wide boxes of 64 k-rows
-              tma_load_2d_pair(sa, &tmA, fb, row0, k * 64);
-              tma_load_2d_pair(sa + 8192, &tmA, fb, row0 + 64, k * 64);
+            constexpr int TK = Cf::kTileK, AT = Cf::kAtom, BX = Cf::kBoxBytes;
+            if constexpr (kAT) {   // M-major A: AT-wide boxes of TK k-rows
+#pragma unroll
+              for (int j = 0; j < 128 / AT; ++j)
+                tma_load_2d_pair(sa + j * BX, &tmA, fb, row0 + j * AT, k * TK);
             } else {
-              tma_load_2d_pair(sa, &tmA, fb, k * 64, row0);
+              tma_load_2d_pair(sa, &tmA, fb, k * TK, row0);
             }
-            if constexpr (kBT) {   // K-major B: this CTA's 128 columns as rows of 64 k
-              tma_load_2d_pair(sb, &tmB, fb, k * 64, col0);
+            if constexpr (kBT) {   // K-major B: this CTA's 128 columns as rows of TK k
+              tma_load_2d_pair(sb, &tmB, fb, k * TK, col0);
             } else {
-              tma_load_2d_pair(sb, &tmB, fb, col0, k * 64);
-              tma_load_2d_pair(sb + 8192, &tmB, fb, col0 + 64, k * 64);
+#pragma unroll
+              for (int j = 0; j < Cf::kHalfN / AT; ++j)
+                tma_load_2d_pair(sb + j * BX, &tmB, fb, col0 + j * AT, k * TK);
             }
           }
           ++issued;
@@ -341,11 +357,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
           } else {
 #pragma unroll
             for (int j = 0; j < Cf::kMmasPerStage; ++j) {
-              const uint64_t ad = kAT ? smem_desc(a0 + j * 2048, 8192, 1024, kLayoutSwizzle128B)
+              constexpr uint32_t BX = Cf::kBoxBytes, ADV = Cf::kMnAdvance;
+              const uint64_t ad = kAT ? smem_desc(a0 + j * ADV, BX, 1024, kLayoutSwizzle128B)
                                       : smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
               const uint64_t bd = kBT ? smem_desc(b0 + j * 32, 16, 1024, kLayoutSwizzle128B)
-                                      : smem_desc(b0 + j * 2048, 8192, 1024, kLayoutSwizzle128B);
-              mma_f16_pair(d_tmem, ad, bd, Cf::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
+                                      : smem_desc(b0 + j * ADV, BX, 1024, kLayoutSwizzle128B);
+              if constexpr (kF8) {
+                mma_f8_pair(d_tmem, ad, bd, Cf::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
+              } else {
+                mma_f16_pair(d_tmem, ad, bd, Cf::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
+              }
             }
           }
           mma_commit_pair(&empty[stage]);

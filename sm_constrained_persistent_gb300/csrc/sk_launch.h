@@ -18,7 +18,10 @@ enum Kind : int {
   kKindMxN128 = 2,
   kKindBf16Pair = 3,
   kKindMxPair = 4,
-  kNumKinds = 5
+  kKindF8N128 = 5,     // fp8 (E4M3) kinds: plain layout only
+  kKindF8N256 = 6,
+  kKindF8Pair = 7,
+  kNumKinds = 8
 };
 constexpr int kNumLayouts = 4;
 constexpr int kNumVariants = kNumKinds * kNumLayouts;
@@ -26,7 +29,8 @@ constexpr int variant_of(int kind, int layout) { return kind * kNumLayouts + lay
 inline int variant_kind(int v) { return v / kNumLayouts; }
 inline int variant_layout(int v) { return v % kNumLayouts; }
 inline bool variant_is_pair(int v) {
-  return variant_kind(v) == kKindBf16Pair || variant_kind(v) == kKindMxPair;
+  return variant_kind(v) == kKindBf16Pair || variant_kind(v) == kKindMxPair ||
+         variant_kind(v) == kKindF8Pair;
 }
 // the plain (untransposed) layout of each kind
 enum : int {
@@ -57,6 +61,8 @@ cudaError_t setup_bf16_pair(int layout, int* max_clusters);
 cudaError_t launch_bf16_pair(int layout, const Launch& l);
 cudaError_t setup_mx_pair(int* max_clusters);
 cudaError_t launch_mx_pair(const Launch& l);
+cudaError_t setup_f8(int kind, int* ctas_or_clusters);
+cudaError_t launch_f8(int kind, const Launch& l);
 
 // Dynamic shared memory of a variant, in bytes.
 size_t variant_smem_bytes(int variant);

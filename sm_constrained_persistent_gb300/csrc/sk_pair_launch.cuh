@@ -6,9 +6,9 @@
 
 namespace sk {
 
-template <bool kMx, bool kAT, bool kBT>
+template <bool kMx, bool kAT, bool kBT, bool kF8 = false>
 cudaError_t launch_pair_kernel(const Launch& l) {
-  using Cf = PairCfg<kMx, kAT, kBT>;
+  using Cf = PairCfg<kMx, kAT, kBT, kF8>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(l.grid), 1, 1);
   cfg.blockDim = dim3(pair_threads<kMx>(), 1, 1);
@@ -16,14 +16,14 @@ cudaError_t launch_pair_kernel(const Launch& l) {
   cfg.stream = l.stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<kMx, kAT, kBT>, *l.tmA, *l.tmB, *l.tmSfa,
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<kMx, kAT, kBT, kF8>, *l.tmA, *l.tmB, *l.tmSfa,
                             *l.tmSfb, l.args);
 }
 
-template <bool kMx, bool kAT, bool kBT>
+template <bool kMx, bool kAT, bool kBT, bool kF8 = false>
 cudaError_t setup_pair_kernel(int* max_clusters) {
-  using Cf = PairCfg<kMx, kAT, kBT>;
-  cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<kMx, kAT, kBT>,
+  using Cf = PairCfg<kMx, kAT, kBT, kF8>;
+  cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<kMx, kAT, kBT, kF8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cf::kSmemBytes));
   if (e != cudaSuccess) return e;
@@ -31,7 +31,7 @@ cudaError_t setup_pair_kernel(int* max_clusters) {
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(pair_threads<kMx>(), 1, 1);
   cfg.dynamicSmemBytes = Cf::kSmemBytes;
-  e = cudaOccupancyMaxActiveClusters(max_clusters, gemm_pair_kernel<kMx, kAT, kBT>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(max_clusters, gemm_pair_kernel<kMx, kAT, kBT, kF8>, &cfg);
   if (e == cudaSuccess && *max_clusters > 0) return e;
   // Some runtimes want the cluster shape in the query even when the kernel declares it.
   cudaGetLastError();
@@ -42,7 +42,7 @@ cudaError_t setup_pair_kernel(int* max_clusters) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(max_clusters, gemm_pair_kernel<kMx, kAT, kBT>, &cfg);
+  return cudaOccupancyMaxActiveClusters(max_clusters, gemm_pair_kernel<kMx, kAT, kBT, kF8>, &cfg);
 }
 
 }  // namespace sk

@@ -36,7 +36,7 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for required in ["sk_gemm_bf16", "sk_gemm_mxfp4", "sk_stream_status", "sk_workspace_reserve",
                      "sk_workspace_release_all", "sk_status_string", "sk_plan", "sk_plan_segments",
-                     "sk_gemm_bf16_ex", "sk_gemm_mxfp4_ex"]:
+                     "sk_gemm_bf16_ex", "sk_gemm_mxfp4_ex", "sk_gemm_fp8", "sk_gemm_fp8_ex"]:
         assert required in names
 
 
@@ -82,12 +82,31 @@ def test_mxfp4_bad_arguments_are_rejected_before_cuda(lib, args):
     assert st == sk.SK_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("args", [
+    dict(A=None), dict(B=None), dict(C=None), dict(A=P + 1), dict(B=P + 8),
+    dict(K=8), dict(K=40), dict(N=24), dict(M=0), dict(out_dtype=3), dict(mode=7),
+    dict(tile_n=64), dict(tile_m=256, tile_n=128),
+])
+def test_fp8_bad_arguments_are_rejected_before_cuda(lib, args):
+    a = dict(A=P, B=P, C=P, M=10, N=32, K=64, out_dtype=1, mode=2, tile_n=0, tile_m=0)
+    a.update(args)
+    opts = {"tile_n": a["tile_n"], "tile_m": a["tile_m"]}
+    st = sk.sk_gemm_fp8_ex(a["A"], a["B"], None, a["C"], a["out_dtype"], a["M"], a["N"], a["K"],
+                           0, a["mode"], opts, None)
+    assert st == sk.SK_ERR_INVALID_ARG
+    if not args.get("tile_n") and not args.get("tile_m"):
+        st = sk.sk_gemm_fp8(a["A"], a["B"], None, a["C"], a["out_dtype"], a["M"], a["N"], a["K"],
+                            0, a["mode"], None)
+        assert st == sk.SK_ERR_INVALID_ARG
+
+
 def test_valid_call_without_a_gpu_is_unsupported_not_a_crash(lib):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     st = sk.sk_gemm_bf16(P, P, None, P, 1, 64, 64, 64, 0, 2, None)
     assert st == sk.SK_ERR_UNSUPPORTED
+    assert sk.sk_gemm_fp8(P, P, None, P, 1, 64, 64, 64, 0, 2, None) == sk.SK_ERR_UNSUPPORTED
 
 
 def test_options_validation(lib):
@@ -112,6 +131,11 @@ def test_plan_fields_follow_the_schedule_rules(lib):
     assert p.tiles == 225 and p.sk_tiles == 225 % 148 and p.whole_tiles == 148
     p = sk.sk_plan(1, 8192, 8192, 8192, 0, "streamk", 148, {"tile_m": 128})
     assert (p.tile_n, p.tile_k, p.iters) == (128, 256, 32)
+    # fp8: 128-deep k blocks (128 bytes of E4M3 per row per block)
+    p = sk.sk_plan(2, 8192, 8192, 8192, 0, "streamk", 148, {"tile_m": 128})
+    assert (p.tile_n, p.tile_k, p.iters) == (256, 128, 64)      # wide 1-CTA tiles fill 148 SMs
+    p = sk.sk_plan(2, 8192, 8192, 8192, 0, "streamk", 152)
+    assert (p.tile_m, p.tile_n, p.tile_k, p.ctas_per_tile, p.grid) == (256, 256, 128, 2, 76)
     with pytest.raises(sk.SkError):
         sk.sk_plan(0, 0, 8, 8, 0, "dp", 148)
 
