@@ -176,7 +176,8 @@ EncodeTiledFn encode_fn() {
 // 2-D tensor map over a row-major matrix [rows][cols] of `elem` bytes per element, boxes of
 // box_cols x box_rows elements, 128-byte swizzle, zero fill outside the matrix.
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, size_t elem, const void* base,
-               int64_t rows, int64_t cols, uint32_t box_cols, uint32_t box_rows) {
+               int64_t rows, int64_t cols, uint32_t box_cols, uint32_t box_rows,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -184,7 +185,7 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, size_t elem, const vo
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -384,9 +385,10 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
     return st;
   if (++ws->epoch == 0) ws->epoch = 1;
 
-  CUtensorMap tmA, tmB, tmSfa, tmSfb;
+  CUtensorMap tmA, tmB, tmSfa, tmSfb, tmC;
   std::memset(&tmSfa, 0, sizeof(tmSfa));
   std::memset(&tmSfb, 0, sizeof(tmSfb));
+  std::memset(&tmC, 0, sizeof(tmC));
   const uint32_t b_box = pair ? 128u : static_cast<uint32_t>(plan.tile_n);   // B rows per CTA (MXFP4)
   bool ok;
   if (format == 0) {
@@ -405,6 +407,15 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
     ok = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, M, K / 2, 128, kTileM) &&
          encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, N, K / 2, 128, b_box);
   }
+  // The bf16 / fp8 pair kernels store C through boxes of 32 rows x 64 bytes (unswizzled; the
+  // row pitch N x element size is a multiple of 16 bytes for both formats).
+  if (ok && pair && format != 1) {
+    ok = out_dtype == SK_BF16
+             ? encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, M, N, 32, 32,
+                         CU_TENSOR_MAP_SWIZZLE_NONE)
+             : encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, M, N, 16, 32,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
   if (!ok) return SK_ERR_CUDA;
 
   sk::Launch l = {};
@@ -412,6 +423,7 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   l.tmB = &tmB;
   l.tmSfa = &tmSfa;
   l.tmSfb = &tmSfb;
+  l.tmC = &tmC;
   l.grid = static_cast<int>(ctas);
   l.cooperative = streamk && !pair;
   l.stream = stream;

@@ -146,6 +146,102 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch,
   }
 }
 
+// Adds bias[n0 .. n0+32) (those below N) to v.
+__device__ __forceinline__ void add_bias_chunk(const Args& a, int64_t n0, float (&v)[32]) {
+  if (a.bias == nullptr) return;
+  const bool full_chunk = n0 + 32 <= a.N;
+  if (a.out_bf16) {
+    const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(a.bias);
+    if (full_chunk) {
+      const uint4* bp = reinterpret_cast<const uint4*>(bias + n0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 w = __ldg(bp + q);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float2 f = __bfloat1622float2(h[e]);
+          v[8 * q + 2 * e] += f.x;
+          v[8 * q + 2 * e + 1] += f.y;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n0 + j < a.N) v[j] += __bfloat162float(bias[n0 + j]);
+    }
+  } else {
+    const float* bias = static_cast<const float*>(a.bias);
+    if (full_chunk) {
+      const float4* bp = reinterpret_cast<const float4*>(bias + n0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 f = __ldg(bp + q);
+        v[4 * q] += f.x;
+        v[4 * q + 1] += f.y;
+        v[4 * q + 2] += f.z;
+        v[4 * q + 3] += f.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n0 + j < a.N) v[j] += bias[n0 + j];
+    }
+  }
+}
+
+// Stages one piece of C -- 32 rows (one per lane) x 64 bytes -- in `buf` and writes it with a
+// TMA store at column x, row y.  The tensor map clips rows and columns past the matrix edge;
+// a piece that starts past the edge is skipped (returns false).  The caller alternates between
+// two buffers after every issued store, so the most recent pending store used the other one,
+// and a wait for at most one pending group means this buffer's last store has read it.
+__device__ __forceinline__ bool tma_store_piece(const Args& a, const CUtensorMap* tmC,
+                                                uint8_t* buf, int lane, const uint4 (&q)[4],
+                                                int64_t x, int64_t y) {
+  if (x >= a.N || y >= a.M) return false;
+  if (lane == 0) bulk_wait_read<1>();
+  __syncwarp();
+  uint4* dst = reinterpret_cast<uint4*>(buf + lane * 64);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[i] = q[i];
+  fence_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmC, buf, static_cast<int32_t>(x), static_cast<int32_t>(y));
+    bulk_commit();
+  }
+  return true;
+}
+
+// Adds the bias to columns [n0, n0+32) of this warp's 32 rows (rows y .. y+31, one per lane),
+// casts, and stores them through the warp's two 2 KB staging buffers (`stage`, alternating by
+// `buf`): one bf16 piece of 32 columns, or two fp32 pieces of 16.
+__device__ __forceinline__ void store_chunk_tma(const Args& a, const CUtensorMap* tmC,
+                                                uint8_t* stage, int& buf, int lane, int64_t n0,
+                                                int64_t y, float (&v)[32]) {
+  add_bias_chunk(a, n0, v);
+  if (a.out_bf16) {
+    uint4 q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q[i]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(v[8 * i + 2 * e], v[8 * i + 2 * e + 1]);
+    }
+    if (tma_store_piece(a, tmC, stage + buf * 2048, lane, q, n0, y)) buf ^= 1;
+  } else {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint4 q[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        q[i] = make_uint4(__float_as_uint(v[16 * hf + 4 * i]), __float_as_uint(v[16 * hf + 4 * i + 1]),
+                          __float_as_uint(v[16 * hf + 4 * i + 2]), __float_as_uint(v[16 * hf + 4 * i + 3]));
+      if (tma_store_piece(a, tmC, stage + buf * 2048, lane, q, n0 + 16 * hf, y)) buf ^= 1;
+    }
+  }
+}
+
 // Adds the bias, casts and stores 32 consecutive columns [n0, n0+32) of row m.
 __device__ __forceinline__ void store_row_chunk(const Args& a, int64_t m, int64_t n0,
                                                 float (&v)[32]) {

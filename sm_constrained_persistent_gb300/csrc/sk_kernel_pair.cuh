@@ -154,6 +154,10 @@ struct PairCfg {
   static constexpr int kStageSfb = kMx ? 2048 : 0;       // all 256 columns, 2 k groups
   static constexpr int kStageBytes = kStageA + kStageB + kStageSfa + kStageSfb;
   static constexpr int kStages = (212 * 1024) / kStageBytes;
+  // bf16 / fp8 results leave through TMA stores: each epilogue warp stages 32 rows x 64 bytes
+  // of C in one of its two 2 KB buffers.  (MXFP4 keeps its scale-factor slots instead.)
+  static constexpr bool kTmaStore = !kMx;
+  static constexpr int kEpiBytes = kTmaStore ? 8 * 2 * 2048 : 0;
   static constexpr int kAccBufs = kMx ? 1 : 2;
   static constexpr uint32_t kAccCols = kBN;
   static constexpr uint32_t kSfaCols = 8;
@@ -162,9 +166,9 @@ struct PairCfg {
   static_assert(kAccBufs * kAccCols + (kMx ? kStages * (kSfaCols + kSfbCols) : 0) <= kTmemCols,
                 "tensor memory budget");
   static constexpr int kBarrierBytes = 512;
-  static_assert((3 * kStages + 6) * 8 + 16 <= kBarrierBytes, "barrier area");
+  static_assert((3 * kStages + 6) * 8 + 20 <= kBarrierBytes, "barrier area");
   static constexpr size_t kSmemBytes =
-      1024 + static_cast<size_t>(kStages) * kStageBytes + kBarrierBytes;
+      1024 + static_cast<size_t>(kStages) * kStageBytes + kEpiBytes + kBarrierBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr uint32_t kIdesc =
       kMx ? ((1u << 7) | (1u << 10) | (1u << 23) | (uint32_t(kBN >> 3) << 17) |
@@ -179,7 +183,8 @@ template <bool kMx, bool kAT = false, bool kBT = false, bool kF8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSfa,
-                     const __grid_constant__ CUtensorMap tmSfb, const __grid_constant__ Args args) {
+                     const __grid_constant__ CUtensorMap tmSfb,
+                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Args args) {
   using Cf = PairCfg<kMx, kAT, kBT, kF8>;
   constexpr int S = Cf::kStages;
   constexpr int kBN = Cf::kBN;
@@ -190,7 +195,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
   uint8_t* ring_b = ring_a + S * Cf::kStageA;
   uint8_t* ring_sfa = ring_b + S * Cf::kStageB;
   uint8_t* ring_sfb = ring_sfa + S * Cf::kStageSfa;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ring_sfb + S * Cf::kStageSfb);
+  uint8_t* epi_stage = ring_sfb + S * Cf::kStageSfb;   // 1 KB aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + Cf::kEpiBytes);
   uint64_t* full = bars;                 // leader: both CTAs' bytes of a stage
   uint64_t* empty = bars + S;            // each CTA: its stage may be refilled
   uint64_t* tfull = bars + 2 * S;        // each CTA: accumulator b is ready
@@ -201,6 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cp_done + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* unit_status = tmem_slot + 2;   // two slots, indexed by unit parity
+  volatile uint32_t* staged_status = tmem_slot + 4; // partials staged in tensor memory
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -439,9 +446,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
     int acc = 0;
     uint32_t acc_phase = 0;
     int parity = 0;
+    uint8_t* my_stage = epi_stage + (warp - 2) * 4096;   // this warp's two staging buffers
+    int sbuf = 0;
     Cursor cur(plan, pair);
     Unit u;
     while (cur.next(plan, u)) {
+      // where this piece's rows and columns lie (worked out before the waits below)
+      int32_t tm, tn;
+      tile_coords(plan, u.tile, tm, tn);
+      const int64_t y_warp = static_cast<int64_t>(tm) * 256 + rank * 128 + quarter * 32;
+      const int64_t m = y_warp + lane;
+      const int64_t n_half = static_cast<int64_t>(tn) * kBN + half * 128;
+      bool has_next;
+      {
+        Cursor peek = cur;
+        Unit later;
+        has_next = peek.next(plan, later);
+      }
       int n_contrib = 0;
       if (u.role == kRoleOwner) {
         int64_t covered = u.k1;
@@ -450,11 +471,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
           covered += (len < plan.iters - covered) ? len : (plan.iters - covered);
         }
       }
+      // A shared tile that is this CTA's last piece: while its k-loop still runs, the
+      // partials of the CTAs that continue it are summed into the idle accumulator, so the
+      // fix-up after the loop reads tensor memory instead of waiting on global memory.  (The
+      // idle accumulator held the previous piece, already drained; no later piece uses it.)
+      const bool staged = Cf::kAccBufs == 2 && u.role == kRoleOwner && !has_next && n_contrib > 0;
+      uint32_t flag_status = kUnitStore;
+      if (staged) {
+        if (et == 0) {
+          uint32_t st = kUnitStore;
+          for (int c = 0; c < n_contrib; ++c) {
+            uint32_t* f = args.flags + 2 * (pair + 1 + c) + rank;
+            if (!wait_flag(f, args.epoch, args.timeout_ns)) {
+              record_error(args, kSiteFlag, u.tile);
+              st = kUnitSkip;
+              break;
+            }
+            *reinterpret_cast<volatile uint32_t*>(f) = 0u;
+          }
+          *staged_status = st;
+        }
+        named_barrier_sync(1, kPairEpilogueThreads);
+        flag_status = *staged_status;
+        if (flag_status == kUnitStore) {
+          const uint32_t t_stage = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(acc ^ 1) * Cf::kAccCols + half * 128;
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
+            const float4* src0 =
+                reinterpret_cast<const float4*>(args.P + (2 * (pair + 1) + rank) * (kBM * kBN)) +
+                static_cast<int64_t>(half * 4 + ch) * 8 * kBM + row;
+            float sum[32];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 p = __ldcg(src0 + q * kBM);
+              sum[4 * q] = p.x;
+              sum[4 * q + 1] = p.y;
+              sum[4 * q + 2] = p.z;
+              sum[4 * q + 3] = p.w;
+            }
+#pragma unroll 1
+            for (int c = 1; c < n_contrib; ++c) {
+              const float4* src = src0 + static_cast<int64_t>(2 * c) * (kBM * kBN / 4);
+              float4 p[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) p[q] = __ldcg(src + q * kBM);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                sum[4 * q] += p[q].x;
+                sum[4 * q + 1] += p[q].y;
+                sum[4 * q + 2] += p[q].z;
+                sum[4 * q + 3] += p[q].w;
+              }
+            }
+            __syncwarp();
+            tmem_store_32cols(t_stage + ch * 32, sum);
+          }
+          tmem_store_wait();
+        }
+      }
       if (et == 0) {
         uint32_t status = kUnitStore;
         if (!wait_bar(&tfull[acc], acc_phase, abort_flag, args, kSiteEpilogue)) {
           status = kUnitAbort;
-        } else if (u.role == kRoleOwner) {
+        } else if (u.role == kRoleOwner && !staged) {
           for (int c = 0; c < n_contrib; ++c) {
             uint32_t* f = args.flags + 2 * (pair + 1 + c) + rank;
             if (!wait_flag(f, args.epoch, args.timeout_ns)) {
@@ -471,10 +551,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
       const uint32_t status = unit_status[parity];
       if (status == kUnitAbort) break;
       tc_fence_after();
-
-      // Drain this thread's 128 columns, then hand the accumulator back.
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc) * Cf::kAccCols + half * 128;
+
+      if (staged) {
+        // Last piece: no later piece waits for this accumulator, so add and store it 32
+        // columns at a time, then release it as usual.
+        const bool store = status == kUnitStore && flag_status == kUnitStore;
+        const uint32_t t_stage = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                 static_cast<uint32_t>(acc ^ 1) * Cf::kAccCols + half * 128;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t own[32], part[32];
+          __syncwarp();
+          tmem_load_32cols(t_row + ch * 32, own);
+          tmem_load_32cols(t_stage + ch * 32, part);
+          tmem_load_wait();
+          float w[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(own[j]) + __uint_as_float(part[j]);
+          if (store) {
+            if constexpr (Cf::kTmaStore) {
+              store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
+            } else {
+              store_row_chunk(args, m, n_half + ch * 32, w);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) remote_arrive(tempty_leader0 + acc * 8);
+        break;   // the last piece
+      }
+
+      // Drain this thread's 128 columns, then hand the accumulator back.
       float v[128];
       __syncwarp();
       tmem_load_64cols(t_row, reinterpret_cast<uint32_t*>(v));
@@ -484,10 +594,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
       __syncwarp();
       if (lane == 0) remote_arrive(tempty_leader0 + acc * 8);
 
-      int32_t tm, tn;
-      tile_coords(plan, u.tile, tm, tn);
-      const int64_t m = static_cast<int64_t>(tm) * 256 + rank * 128 + row;
-      const int64_t n_half = static_cast<int64_t>(tn) * kBN + half * 128;
       if (u.role == kRoleContrib) {
         float4* dst = reinterpret_cast<float4*>(args.P + cta * (kBM * kBN)) +
                       static_cast<int64_t>(half * 4) * 8 * kBM + row;
@@ -519,14 +625,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
           }
         }
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-          store_row_chunk(args, m, n_half + ch * 32, *reinterpret_cast<float(*)[32]>(&v[ch * 32]));
+        for (int ch = 0; ch < 4; ++ch) {
+          float(&w)[32] = *reinterpret_cast<float(*)[32]>(&v[ch * 32]);
+          if constexpr (Cf::kTmaStore) {
+            store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
+          } else {
+            store_row_chunk(args, m, n_half + ch * 32, w);
+          }
+        }
       }
       parity ^= 1;
       if (++acc == Cf::kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
       }
+    }
+    if constexpr (Cf::kTmaStore) {
+      if (lane == 0) bulk_wait_all();   // staged pieces are read and written before exit
     }
   }
 
