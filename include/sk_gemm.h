@@ -161,6 +161,36 @@ sk_status_t sk_gemm_fp8_ex(const void* A, const void* B, const void* bias, void*
                            sk_mode_t mode, const sk_options_t* options, void* stream);
 
 /*
+ * sk_gemm_bf16_host / sk_gemm_fp8_host / sk_gemm_mxfp4_host — the same addmm for operands and
+ * result in HOST memory (the pages' calls take device tensors; this is the path for a caller
+ * whose data lives on the host).  Arguments as the _ex calls, except that A, A_scale, B,
+ * B_scale, bias and C are host pointers.  Page-locked (pinned) host memory lets the copies
+ * overlap the computation; pageable memory works but copies synchronously.
+ *   - The library keeps device copies of the operands and two copy streams per (device,
+ *     stream), grown on demand and freed by sk_workspace_release_all.
+ *   - B, its scales and the bias are copied first; A (and its scales) follows in up to 8
+ *     row blocks of a multiple of 256 rows.  Each block's GEMM starts on `stream` when its
+ *     rows have arrived, and its rows of C are copied back while later blocks compute.
+ *   - Asynchronous like the other calls: C is complete once `stream` reaches the point after
+ *     this call (synchronise it before reading C).  The host buffers must stay valid until then.
+ *   - Shape, option and dtype errors are reported before anything is copied.  Refused
+ *     (SK_ERR_UNSUPPORTED) while `stream` is being captured.
+ */
+sk_status_t sk_gemm_bf16_host(const void* A, const void* B, const void* bias, void* C,
+                              sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
+                              sk_mode_t mode, const sk_options_t* options, void* stream);
+
+sk_status_t sk_gemm_fp8_host(const void* A, const void* B, const void* bias, void* C,
+                             sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
+                             sk_mode_t mode, const sk_options_t* options, void* stream);
+
+sk_status_t sk_gemm_mxfp4_host(const void* A, const void* A_scale, const void* B,
+                               const void* B_scale, const void* bias, void* C,
+                               sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K,
+                               int num_sms, sk_mode_t mode, const sk_options_t* options,
+                               void* stream);
+
+/*
  * sk_gemm_bf16_t — C[M x N] = op(A) * op(B) (+ bias[N]) with either bf16 operand stored
  * transposed, through the same schedules and kernels (operands read M-major / K-major by the
  * tensor cores, no copy).

@@ -86,6 +86,13 @@ def lib():
             h.sk_gemm_fp8_ex.restype = i32
             h.sk_gemm_fp8_ex.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, i32,
                                          ctypes.POINTER(Options), vp]
+            for name in ("sk_gemm_bf16_host", "sk_gemm_fp8_host"):
+                getattr(h, name).restype = i32
+                getattr(h, name).argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, i32,
+                                             ctypes.POINTER(Options), vp]
+            h.sk_gemm_mxfp4_host.restype = i32
+            h.sk_gemm_mxfp4_host.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, i32, i32,
+                                             ctypes.POINTER(Options), vp]
             h.sk_gemm_bf16_t.restype = i32
             h.sk_gemm_bf16_t.argtypes = [vp, i32, vp, i32, vp, vp, i32, i64, i64, i64, i32, i32,
                                          ctypes.POINTER(Options), vp]
@@ -154,6 +161,22 @@ def sk_gemm_fp8(A, B, bias, C, out_dtype, M, N, K, num_sms, mode, stream):
 def sk_gemm_fp8_ex(A, B, bias, C, out_dtype, M, N, K, num_sms, mode, options, stream):
     return lib().sk_gemm_fp8_ex(A, B, bias, C, out_dtype, M, N, K, num_sms, mode,
                                 _opts(options), stream)
+
+
+def sk_gemm_bf16_host(A, B, bias, C, out_dtype, M, N, K, num_sms, mode, options, stream):
+    return lib().sk_gemm_bf16_host(A, B, bias, C, out_dtype, M, N, K, num_sms, mode,
+                                   _opts(options), stream)
+
+
+def sk_gemm_fp8_host(A, B, bias, C, out_dtype, M, N, K, num_sms, mode, options, stream):
+    return lib().sk_gemm_fp8_host(A, B, bias, C, out_dtype, M, N, K, num_sms, mode,
+                                  _opts(options), stream)
+
+
+def sk_gemm_mxfp4_host(A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sms, mode,
+                       options, stream):
+    return lib().sk_gemm_mxfp4_host(A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sms,
+                                    mode, _opts(options), stream)
 
 
 def sk_gemm_bf16_t(A, trans_a, B, trans_b, bias, C, out_dtype, M, N, K, num_sms, mode, options,
@@ -304,6 +327,45 @@ def gemm_fp8(a, b, bias=None, out=None, out_dtype=None, num_sms=0, mode="streamk
                         out.data_ptr(), od, M, N, K, num_sms, _mode(mode), options,
                         _stream_ptr(stream))
     _check(st, "sk_gemm_fp8")
+    return out
+
+
+def gemm_host(fmt, a, b, bias=None, out=None, out_dtype=None, a_scale=None, b_scale=None,
+              num_sms=0, mode="streamk", options=None, stream=None):
+    """The addmm on host (CPU) tensors, ideally pinned: fmt "bf16" (a (M,K), b (K,N) bf16),
+    "fp8" (a (M,K), b (K,N) float8_e4m3fn or uint8 codes) or "mxfp4" (a (M,K/2), b (N,K/2)
+    uint8 codes with E8M0 scales).  Copies in, computes and copies out on the given (or current)
+    CUDA stream; synchronises that stream before returning C."""
+    import torch
+    tensors = [a, b] + [t for t in (bias, out, a_scale, b_scale) if t is not None]
+    for t in tensors:
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous host tensors")
+    if fmt == "mxfp4":
+        M, K, N = a.shape[0], a.shape[1] * 2, b.shape[0]
+    else:
+        (M, K), N = a.shape, b.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, pin_memory=True)
+    od = SK_BF16 if out.dtype == torch.bfloat16 else SK_F32
+    if bias is not None and bias.dtype != out.dtype:
+        raise TypeError("bias must have the output dtype")
+    bp = bias.data_ptr() if bias is not None else None
+    s = torch.cuda.current_stream() if stream is None else stream
+    if fmt == "bf16":
+        st = sk_gemm_bf16_host(a.data_ptr(), b.data_ptr(), bp, out.data_ptr(), od, M, N, K,
+                               num_sms, _mode(mode), options, s.cuda_stream)
+    elif fmt == "fp8":
+        st = sk_gemm_fp8_host(a.data_ptr(), b.data_ptr(), bp, out.data_ptr(), od, M, N, K,
+                              num_sms, _mode(mode), options, s.cuda_stream)
+    elif fmt == "mxfp4":
+        st = sk_gemm_mxfp4_host(a.data_ptr(), a_scale.data_ptr(), b.data_ptr(),
+                                b_scale.data_ptr(), bp, out.data_ptr(), od, M, N, K, num_sms,
+                                _mode(mode), options, s.cuda_stream)
+    else:
+        raise ValueError(fmt)
+    _check(st, f"sk_gemm_{fmt}_host")
+    s.synchronize()
     return out
 
 

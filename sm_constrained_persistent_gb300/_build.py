@@ -18,7 +18,7 @@ LIB_DIR = os.path.join(_PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libskgemm.so")
 SOURCES = ["sk_api.cu", "sk_kernel_bf16.cu", "sk_kernel_bf16_wide.cu", "sk_kernel_mxfp4.cu",
            "sk_kernel_pair.cu", "sk_kernel_pair_mx.cu", "sk_kernel_fp8.cu", "sk_reduce.cu",
-           "sk_static.cu"]
+           "sk_static.cu", "sk_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

@@ -635,6 +635,7 @@ void sk_workspace_release_all(void) {
   }
   g_workspaces.clear();
   cudaSetDevice(prev);
+  sk::release_host_stages();
 }
 
 const char* sk_status_string(sk_status_t s) {

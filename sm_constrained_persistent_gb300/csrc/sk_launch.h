@@ -65,6 +65,9 @@ cudaError_t launch_mx_pair(const Launch& l);
 cudaError_t setup_f8(int kind, int* ctas_or_clusters);
 cudaError_t launch_f8(int kind, const Launch& l);
 
+// Frees the device copies, streams and events of the host-buffer entry points.
+void release_host_stages();
+
 // Dynamic shared memory of a variant, in bytes.
 size_t variant_smem_bytes(int variant);
 // Raises the variant's dynamic shared-memory limit on the current device and reports how many

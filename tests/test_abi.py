@@ -36,7 +36,8 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for required in ["sk_gemm_bf16", "sk_gemm_mxfp4", "sk_stream_status", "sk_workspace_reserve",
                      "sk_workspace_release_all", "sk_status_string", "sk_plan", "sk_plan_segments",
-                     "sk_gemm_bf16_ex", "sk_gemm_mxfp4_ex", "sk_gemm_fp8", "sk_gemm_fp8_ex"]:
+                     "sk_gemm_bf16_ex", "sk_gemm_mxfp4_ex", "sk_gemm_fp8", "sk_gemm_fp8_ex",
+                     "sk_gemm_bf16_host", "sk_gemm_fp8_host", "sk_gemm_mxfp4_host"]:
         assert required in names
 
 
@@ -98,6 +99,24 @@ def test_fp8_bad_arguments_are_rejected_before_cuda(lib, args):
         st = sk.sk_gemm_fp8(a["A"], a["B"], None, a["C"], a["out_dtype"], a["M"], a["N"], a["K"],
                             0, a["mode"], None)
         assert st == sk.SK_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("fmt,args", [
+    ("bf16", dict(A=None)), ("bf16", dict(C=None)), ("bf16", dict(K=100)), ("bf16", dict(N=20)),
+    ("bf16", dict(M=0)), ("bf16", dict(out_dtype=2)), ("fp8", dict(K=40)), ("fp8", dict(N=24)),
+    ("mxfp4", dict(K=48)), ("mxfp4", dict(A_scale=None)),
+])
+def test_host_buffer_calls_reject_bad_arguments_before_copying(lib, fmt, args):
+    a = dict(A=P, A_scale=P, B=P, B_scale=P, C=P, M=64, N=64, K=64, out_dtype=1)
+    a.update(args)
+    common = (a["C"], a["out_dtype"], a["M"], a["N"], a["K"], 0, 2, None, None)
+    if fmt == "bf16":
+        st = sk.sk_gemm_bf16_host(a["A"], a["B"], None, *common)
+    elif fmt == "fp8":
+        st = sk.sk_gemm_fp8_host(a["A"], a["B"], None, *common)
+    else:
+        st = sk.sk_gemm_mxfp4_host(a["A"], a["A_scale"], a["B"], a["B_scale"], None, *common)
+    assert st == sk.SK_ERR_INVALID_ARG
 
 
 def test_valid_call_without_a_gpu_is_unsupported_not_a_crash(lib):
