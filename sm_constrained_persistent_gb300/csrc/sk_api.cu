@@ -407,9 +407,11 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
     ok = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, M, K / 2, 128, kTileM) &&
          encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, N, K / 2, 128, b_box);
   }
-  // The bf16 / fp8 pair kernels store C through boxes of 32 rows x 64 bytes (unswizzled; the
-  // row pitch N x element size is a multiple of 16 bytes for both formats).
-  if (ok && pair && format != 1) {
+  // C leaves through TMA stores of 32 rows x 64 bytes (unswizzled) when its row pitch is a
+  // multiple of 16 bytes: always for bf16 and fp8 operands (N % 8 == 0), and for MXFP4 when N
+  // allows.  The MXFP4 pair kernel has no room for the staging buffers and stores directly.
+  const bool c_tma = (out_dtype == SK_BF16 ? N % 8 == 0 : N % 4 == 0) && !(pair && format == 1);
+  if (ok && c_tma) {
     ok = out_dtype == SK_BF16
              ? encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, M, N, 32, 32,
                          CU_TENSOR_MAP_SWIZZLE_NONE)
@@ -423,7 +425,7 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   l.tmB = &tmB;
   l.tmSfa = &tmSfa;
   l.tmSfb = &tmSfb;
-  l.tmC = &tmC;
+  l.tmC = c_tma ? &tmC : nullptr;
   l.grid = static_cast<int>(ctas);
   l.cooperative = streamk && !pair;
   l.stream = stream;
@@ -441,6 +443,7 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   a.P = ws->P;
   a.flags = ws->flags;
   a.err = ws->err;
+  a.c_tma = c_tma ? 1 : 0;
   a.timeout_ns = static_cast<uint64_t>(
       opt != nullptr && opt->spin_timeout_ns > 0 ? opt->spin_timeout_ns : kDefaultTimeoutNs);
   if (format == 1) {

@@ -81,8 +81,12 @@ struct Cfg {
   static_assert(2 * kAccCols + (kMx ? kStages * (kSfaCols + kSfbCols) : 0) <= kTmemCols,
                 "tensor memory budget");
   static constexpr int kBarrierBytes = 256;
+  static_assert((2 * kStages + 5) * 8 + 20 <= kBarrierBytes, "barrier area");
+  // C leaves through TMA stores when its rows are 16-byte aligned: each epilogue warp stages
+  // 32 rows x 64 bytes in one of its two 2 KB buffers.
+  static constexpr int kEpiBytes = 4 * 2 * 2048;
   static constexpr size_t kSmemBytes =
-      1024 + static_cast<size_t>(kStages) * kStageBytes + kBarrierBytes;
+      1024 + static_cast<size_t>(kStages) * kStageBytes + kEpiBytes + kBarrierBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   // Instruction descriptor: fp32 D; bf16: bf16 A/B, A K-major (M-major when kAT, bit 15),
   // B MN-major (K-major when kBT, bit 16 clear); MXFP4: E2M1 A/B, E8M0 scales, both K-major.
@@ -314,7 +318,7 @@ __device__ __forceinline__ void store_row_chunk(const Args& a, int64_t m, int64_
 template <bool kMx, int kBN, bool kAT = false, bool kBT = false, bool kF8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ Args args) {
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Args args) {
   using Cf = Cfg<kMx, kBN, kAT, kBT, kF8>;
   constexpr int S = Cf::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -324,7 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ring_b = ring_a + S * Cf::kStageA;
   uint8_t* ring_sfa = ring_b + S * Cf::kStageB;
   uint8_t* ring_sfb = ring_sfa + S * Cf::kStageSfa;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ring_sfb + S * Cf::kStageSfb);
+  uint8_t* epi_stage = ring_sfb + S * Cf::kStageSfb;   // 1 KB aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + Cf::kEpiBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* tfull = bars + 2 * S;
@@ -333,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* unit_status = tmem_slot + 2;   // two slots, indexed by accumulator
+  volatile uint32_t* staged_status = tmem_slot + 4; // partials staged in tensor memory
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -531,9 +537,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = threadIdx.x - 64;            // 0..127
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint8_t* my_stage = epi_stage + (warp - 2) * 4096;   // this warp's two C staging buffers
+    int sbuf = 0;
     Cursor cur(plan, cta);
     Unit u;
     while (cur.next(plan, u)) {
+      // where this piece's rows and columns lie (worked out before the waits below)
+      int32_t tm, tn;
+      tile_coords(plan, u.tile, tm, tn);
+      const int64_t y_warp = static_cast<int64_t>(tm) * kBM + quarter * 32;
+      const int64_t m = y_warp + lane;
+      const int64_t n_tile = static_cast<int64_t>(tn) * kBN;
+      bool has_next;
+      {
+        Cursor peek = cur;
+        Unit later;
+        has_next = peek.next(plan, later);
+      }
       // Contributions to an owned tile come from CTAs cta+1, cta+2, ... until k is covered.
       int n_contrib = 0;
       if (u.role == kRoleOwner) {
@@ -543,11 +563,69 @@ __global__ void __launch_bounds__(kThreads, 1)
           covered += (len < plan.iters - covered) ? len : (plan.iters - covered);
         }
       }
+      // A shared tile that is this CTA's last piece: while its k-loop still runs, the
+      // contributors' partials are summed into the idle accumulator (which held the previous
+      // piece, already drained; no later piece uses it), so the fix-up after the loop reads
+      // tensor memory instead of waiting on global memory.
+      const bool staged = u.role == kRoleOwner && !has_next && n_contrib > 0;
+      const uint32_t t_stage = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               static_cast<uint32_t>(acc ^ 1) * Cf::kAccCols;
+      uint32_t flag_status = kUnitStore;
+      if (staged) {
+        if (et == 0) {
+          uint32_t st = kUnitStore;
+          for (int c = 0; c < n_contrib; ++c) {
+            uint32_t* f = args.flags + cta + 1 + c;
+            if (!wait_flag(f, args.epoch, args.timeout_ns)) {
+              record_error(args, kSiteFlag, u.tile);
+              st = kUnitSkip;
+              break;
+            }
+            *reinterpret_cast<volatile uint32_t*>(f) = 0u;  // consumed: ready for the next launch
+          }
+          *staged_status = st;
+        }
+        named_barrier_sync(1, kEpilogueThreads);
+        flag_status = *staged_status;
+        if (flag_status == kUnitStore) {
+#pragma unroll 1
+          for (int ch = 0; ch < kBN / 32; ++ch) {
+            const float4* src0 = reinterpret_cast<const float4*>(args.P + (cta + 1) * (kBM * kBN)) +
+                                 static_cast<int64_t>(ch) * 8 * kBM + row;
+            float sum[32];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 p = __ldcg(src0 + q * kBM);
+              sum[4 * q] = p.x;
+              sum[4 * q + 1] = p.y;
+              sum[4 * q + 2] = p.z;
+              sum[4 * q + 3] = p.w;
+            }
+#pragma unroll 1
+            for (int c = 1; c < n_contrib; ++c) {
+              const float4* src = src0 + static_cast<int64_t>(c) * (kBM * kBN / 4);
+              float4 p[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) p[q] = __ldcg(src + q * kBM);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                sum[4 * q] += p[q].x;
+                sum[4 * q + 1] += p[q].y;
+                sum[4 * q + 2] += p[q].z;
+                sum[4 * q + 3] += p[q].w;
+              }
+            }
+            __syncwarp();
+            tmem_store_32cols(t_stage + ch * 32, sum);
+          }
+          tmem_store_wait();
+        }
+      }
       if (et == 0) {
         uint32_t status = kUnitStore;
         if (!wait_bar(&tfull[acc], acc_phase, abort_flag, args, kSiteEpilogue)) {
           status = kUnitAbort;
-        } else if (u.role == kRoleOwner) {
+        } else if (u.role == kRoleOwner && !staged) {
           for (int c = 0; c < n_contrib; ++c) {
             uint32_t* f = args.flags + cta + 1 + c;
             if (!wait_flag(f, args.epoch, args.timeout_ns)) {
@@ -564,11 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t status = unit_status[acc];
       if (status == kUnitAbort) break;
       tc_fence_after();
-      int32_t tm, tn;
-      tile_coords(plan, u.tile, tm, tn);
-      const int64_t m = static_cast<int64_t>(tm) * kBM + row;
-      const int64_t n_tile = static_cast<int64_t>(tn) * kBN;
-      const bool do_store = (status == kUnitStore);
+      const bool do_store = status == kUnitStore && flag_status == kUnitStore;
 
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc) * Cf::kAccCols;
@@ -576,11 +650,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int ch = 0; ch < kBN / 32; ++ch) {
         uint32_t r[32];
+        __syncwarp();
         tmem_load_32cols(t_row + ch * 32, r);
-        tmem_load_wait();
         float v[32];
+        if (staged) {
+          uint32_t part[32];
+          tmem_load_32cols(t_stage + ch * 32, part);
+          tmem_load_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) + __uint_as_float(part[j]);
+        } else {
+          tmem_load_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        }
         if (u.role == kRoleContrib) {
           // Slot layout [chunk][column quad][row]: one warp store covers 512 contiguous bytes.
           float4* dst = my_slot + static_cast<int64_t>(ch) * 8 * kBM + row;
@@ -588,19 +671,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 8; ++q)
             __stcg(dst + q * kBM, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
         } else if (do_store) {
-          for (int c = 0; c < n_contrib; ++c) {
-            const float4* src = reinterpret_cast<const float4*>(args.P + (cta + 1 + c) * (kBM * kBN)) +
-                                static_cast<int64_t>(ch) * 8 * kBM + row;
+          if (!staged) {
+            for (int c = 0; c < n_contrib; ++c) {
+              const float4* src =
+                  reinterpret_cast<const float4*>(args.P + (cta + 1 + c) * (kBM * kBN)) +
+                  static_cast<int64_t>(ch) * 8 * kBM + row;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 p = __ldcg(src + q * kBM);
-              v[4 * q] += p.x;
-              v[4 * q + 1] += p.y;
-              v[4 * q + 2] += p.z;
-              v[4 * q + 3] += p.w;
+              for (int q = 0; q < 8; ++q) {
+                const float4 p = __ldcg(src + q * kBM);
+                v[4 * q] += p.x;
+                v[4 * q + 1] += p.y;
+                v[4 * q + 2] += p.z;
+                v[4 * q + 3] += p.w;
+              }
             }
           }
-          store_row_chunk(args, m, n_tile + ch * 32, v);
+          if (args.c_tma) {
+            store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_tile + ch * 32, y_warp, v);
+          } else {
+            store_row_chunk(args, m, n_tile + ch * 32, v);
+          }
         }
       }
       // Accumulator drained: hand it back to the MMA warp.
@@ -617,6 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) bulk_wait_all();   // staged pieces of C are read and written before exit
   }
 
   tc_fence_before();

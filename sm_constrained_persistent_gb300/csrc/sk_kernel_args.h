@@ -23,6 +23,8 @@ struct Args {
   const uint8_t* sfa;    // MXFP4 scales, rearranged: [row block][k group][512 bytes]
   const uint8_t* sfb;
   int64_t sf_kgroups;    // k groups (4 scale blocks = 128 K elements each) per row block
+  int32_t c_tma;         // one-CTA kernels: 1 = C is written through the tmC tensor map
+  int32_t pad_;
 };
 
 }  // namespace sk

@@ -18,7 +18,8 @@ static cudaError_t launch_one(const Launch& l) {
   attr[0].val.cooperative = l.cooperative ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<false, 128, kAT, kBT>, *l.tmA, *l.tmB, l.args);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<false, 128, kAT, kBT>, *l.tmA, *l.tmB,
+                            l.tmC != nullptr ? *l.tmC : *l.tmA, l.args);
 }
 
 template <bool kAT, bool kBT>

@@ -19,7 +19,7 @@ static cudaError_t launch_f8_one(const Launch& l) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemm_kernel<false, kBN, false, false, true>, *l.tmA, *l.tmB,
-                            l.args);
+                            l.tmC != nullptr ? *l.tmC : *l.tmA, l.args);
 }
 
 template <int kBN>

@@ -96,7 +96,8 @@ cudaError_t variant_launch(int variant, const Launch& l) {
       attr[0].val.cooperative = l.cooperative ? 1 : 0;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      return cudaLaunchKernelEx(&cfg, gemm_kernel<true, 128>, *l.tmA, *l.tmB, l.args);
+      return cudaLaunchKernelEx(&cfg, gemm_kernel<true, 128>, *l.tmA, *l.tmB,
+                            l.tmC != nullptr ? *l.tmC : *l.tmA, l.args);
     }
     case kKindF8N128:
     case kKindF8N256: return launch_f8(variant_kind(variant), l);

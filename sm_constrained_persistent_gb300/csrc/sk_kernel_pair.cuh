@@ -571,7 +571,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
 #pragma unroll
           for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(own[j]) + __uint_as_float(part[j]);
           if (store) {
-            if constexpr (Cf::kTmaStore) {
+            if (Cf::kTmaStore && args.c_tma) {
               store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else {
               store_row_chunk(args, m, n_half + ch * 32, w);
@@ -627,7 +627,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           float(&w)[32] = *reinterpret_cast<float(*)[32]>(&v[ch * 32]);
-          if constexpr (Cf::kTmaStore) {
+          if (Cf::kTmaStore && args.c_tma) {
             store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
           } else {
             store_row_chunk(args, m, n_half + ch * 32, w);

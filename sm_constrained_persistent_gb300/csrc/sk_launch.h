@@ -46,7 +46,8 @@ struct Launch {
   const CUtensorMap* tmB;
   const CUtensorMap* tmSfa;   // pair MXFP4 only: rearranged scales as rows of 1 KB
   const CUtensorMap* tmSfb;
-  const CUtensorMap* tmC;     // pair bf16 / fp8 only: C as 32 rows x 64 bytes boxes
+  const CUtensorMap* tmC;     // C as boxes of 32 rows x 64 bytes (null: no TMA stores; the
+                              // one-CTA kernels then store directly, args.c_tma = 0)
   Args args;
   int grid;
   bool cooperative;   // ask the driver to guarantee that every CTA is resident at once

@@ -17,7 +17,7 @@ cudaError_t launch_pair_kernel(const Launch& l) {
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
   return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<kMx, kAT, kBT, kF8>, *l.tmA, *l.tmB, *l.tmSfa,
-                            *l.tmSfb, *l.tmC, l.args);
+                            *l.tmSfb, l.tmC != nullptr ? *l.tmC : *l.tmA, l.args);
 }
 
 template <bool kMx, bool kAT, bool kBT, bool kF8 = false>
