@@ -46,7 +46,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="addmm_bf16_8192")
-    ap.add_argument("--mode", default="streamk", choices=["dp", "persistent", "streamk", "hybrid"])
+    ap.add_argument("--mode", default="streamk", choices=["dp", "persistent", "streamk", "hybrid", "auto"])
     ap.add_argument("--num-sms", type=int, default=0)
     ap.add_argument("--no-extras", action="store_true", help="skip the per-schedule extras")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -627,6 +627,39 @@ def backward(pr, bf16_peak, steps=10, warmup=3):
     return res
 
 
+# Shapes outside the set the automatic choice's cost model was fitted on.
+AUTO_CHECK_SHAPES = [(3584, 3584, 3584), (1280, 5120, 5120), (640, 2560, 16384),
+                     (7168, 7168, 1536), (96, 8192, 8192), (4864, 1792, 8192)]
+
+
+def auto_selection(device, sm_count, bpeak, dist):
+    """SK_MODE_AUTO against every schedule x tile kind on shapes held out of its calibration:
+    the automatic plan's time, the fastest configuration and the ratio."""
+    from sm_constrained_persistent_gb300 import inputs
+    tiles = {"pair": {"tile_m": 256}, "128x256": {"tile_m": 128, "tile_n": 256},
+             "128x128": {"tile_m": 128, "tile_n": 128}}
+    res = {}
+    for (M, N, K) in AUTO_CHECK_SHAPES:
+        name = f"gemm_bf16_{M}x{N}x{K}"
+        inputs.WORKLOADS.setdefault(name, ("bf16", M, N, K, dict(operand_scale="sqrt_k",
+                                                                 bias="none"), "bf16", 1240))
+        pr = Problem(name, device)
+        auto = _time_modes(pr, ["auto"], sm_count, bpeak, dist)["auto"]
+        best = None
+        for tname, opt in tiles.items():
+            if tname == "pair" and M <= 128:
+                continue
+            for mode, r in _time_modes(pr, ["dp", "persistent", "streamk", "hybrid"], sm_count,
+                                       bpeak, dist, options=opt).items():
+                if best is None or r["ms"] < best["ms"]:
+                    best = dict(r, mode=mode)
+        res[name] = {"auto_ms": auto["ms"], "auto_tile": auto["tile"], "best_ms": best["ms"],
+                     "best": f"{best['mode']} {best['tile']}",
+                     "auto_over_best": round(auto["ms"] / best["ms"], 3)}
+        del pr
+    return res
+
+
 def extras(prob, sm_count, dist):
     """Per-schedule throughput of the benchmark workloads, each timed on its own after the
     headline region (3 warm-up + 10 timed calls per entry), and the SM-constrained sweep."""
@@ -670,6 +703,7 @@ def extras(prob, sm_count, dist):
             rows[str(ns)] = r
         sweep[name] = rows
     out["num_sms_sweep_persistent"] = sweep
+    out["auto_selection"] = auto_selection(prob.device, sm_count, bpeak, dist)
     out["corun_half_sms"] = corun(get("addmm_bf16_8192"), sm_count)
     out["addmm_backward_bf16_8192"] = backward(get("addmm_bf16_8192"), bpeak)
     for name in list(cache):

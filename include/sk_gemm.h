@@ -21,6 +21,15 @@
  *                       mxfp4 kernel": one P slot and one lock per CTA).
  *   SK_MODE_HYBRID      the last (tiles mod g) tiles run Stream-K over all g CTAs (each CTA does
  *                       its Stream-K share first), the other tiles run whole, round-robin.
+ *   SK_MODE_AUTO        the library picks the schedule (persistent, Stream-K or hybrid) and the
+ *                       CTA tile (256 x 256 SM pairs, 128 x 256 or 128 x 128, within any tile
+ *                       the options force) with the lowest estimated time.  The estimate is a
+ *                       cost model fitted to GB300 timings: launch + per-k-iteration time of
+ *                       the tile kind x the iterations of the busiest CTA + a cost per piece of
+ *                       work + a Stream-K fix-up cost per split tile and per CTA sharing it.
+ *                       This is the tuning step the SM-constraint GEMM page lists as optional
+ *                       (flashinfer PR #982, "tune: get best config for gemm").  sk_plan()
+ *                       reports the choice (its `mode` field holds the schedule picked).
  *
  * Conventions shared by every entry point
  *   - Pointers A, B, bias, C, A_scale, B_scale are DEVICE pointers owned by the caller, on the
@@ -53,7 +62,8 @@ typedef enum {
   SK_MODE_DP = 0,
   SK_MODE_PERSISTENT = 1,
   SK_MODE_STREAMK = 2,
-  SK_MODE_HYBRID = 3
+  SK_MODE_HYBRID = 3,
+  SK_MODE_AUTO = 4
 } sk_mode_t;
 
 /* dtype of C, and of bias (the bias always has C's dtype) */

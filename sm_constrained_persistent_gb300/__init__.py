@@ -14,7 +14,7 @@ import threading
 
 from . import _build
 
-MODES = {"dp": 0, "persistent": 1, "streamk": 2, "hybrid": 3}
+MODES = {"dp": 0, "persistent": 1, "streamk": 2, "hybrid": 3, "auto": 4}
 SK_F32, SK_BF16 = 0, 1
 STATUS = {0: "SK_OK", 1: "SK_ERR_INVALID_ARG", 2: "SK_ERR_UNSUPPORTED", 3: "SK_ERR_OOM",
           4: "SK_ERR_CUDA", 5: "SK_ERR_TIMEOUT", 6: "SK_ERR_NOT_CORESIDENT"}

@@ -1,0 +1,113 @@
+"""Calibration of the automatic schedule and tile choice (SK_MODE_AUTO).
+
+`sweep()` times a list of bf16 shapes under every schedule and tile kind on the current GPU;
+`fit()` fits the cost model's constants (the `kCost` table in csrc/sk_api.cu) to such timings
+by non-negative least squares on the relative error, and reports how close the cheapest
+estimate comes to the fastest configuration.  `gb300_bf16_sweep.json` holds the timings the
+shipped constants were fitted to.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+TILES = {"pair": {"tile_m": 256}, "128x256": {"tile_m": 128, "tile_n": 256},
+         "128x128": {"tile_m": 128, "tile_n": 128}}
+MODES = ["dp", "persistent", "streamk", "hybrid"]
+
+
+def load(path=os.path.join(HERE, "gb300_bf16_sweep.json")):
+    with open(path) as f:
+        return json.load(f)["times"]
+
+
+def sweep(shapes, steps=10, warmup=3, seed=99):
+    """{"MxNxK": {tile: {mode: ms}}} for bf16 N(0,1)/sqrt(K) operands on the current device."""
+    import numpy as np
+    import torch
+    import sm_constrained_persistent_gb300 as sk
+    from sm_constrained_persistent_gb300 import inputs
+    flush_w = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
+    flush_r = torch.ones((64 << 10, 1024), dtype=torch.float32, device="cuda")
+    flush_o = torch.empty(1024, dtype=torch.float32, device="cuda")
+    out = {}
+    for (M, N, K) in shapes:
+        p = inputs.bf16_problem(M, N, K, seed=seed, operand_scale="sqrt_k")
+        a = torch.from_numpy(p["A"].view(np.int16)).view(torch.bfloat16).cuda()
+        b = torch.from_numpy(p["B"].view(np.int16)).view(torch.bfloat16).cuda()
+        c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        res = {}
+        for tname, opt in TILES.items():
+            if tname == "pair" and M <= 128:
+                continue
+            res[tname] = {}
+            for mode in MODES:
+                for _ in range(warmup):
+                    sk.gemm_bf16(a, b, out=c, mode=mode, options=opt)
+                total = 0.0
+                for _ in range(steps):
+                    flush_w.fill_(1.0)
+                    torch.amax(flush_r, dim=0, out=flush_o)
+                    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    s.record()
+                    sk.gemm_bf16(a, b, out=c, mode=mode, options=opt)
+                    e.record()
+                    torch.cuda.synchronize()
+                    total += s.elapsed_time(e)
+                sk.stream_status()
+                res[tname][mode] = total / steps
+        out[f"{M}x{N}x{K}"] = res
+    return out
+
+
+def _features(M, N, K, tile, mode, sm_count):
+    import sm_constrained_persistent_gb300 as sk
+    p = sk.sk_plan(0, M, N, K, 0, mode, sm_count, TILES[tile])
+    g, T, I = p.grid, p.tiles, p.iters
+    kind = ["pair", "128x256", "128x128"].index(tile)
+    x = [0.0] * 8
+    if mode in ("dp", "persistent"):
+        workers = min(g, sm_count // p.ctas_per_tile)
+        waves = math.ceil(T / workers)
+        x[kind], x[3] = waves * I, waves
+        x[7] = waves if mode == "dp" else 0
+    else:
+        skT, whole = p.sk_tiles, p.whole_tiles
+        per = math.ceil(skT * I / g) if skT else 0
+        x[kind] = per + math.ceil(whole / g) * I
+        x[3] = math.ceil(whole / g) + (math.ceil(per / I) + 1 if skT else 0)
+        x[4] = 1.0 if skT and (per % I != 0 or (skT * I) % g != 0) else 0.0
+        x[5] = math.ceil(I / per) if skT else 0
+    x[6] = 1.0
+    return x
+
+
+def fit(times, sm_count=152):
+    """Constants (us): per-k-iteration time of a pair / 128x256 / 128x128 tile, per piece,
+    per split region, per CTA sharing a split tile, launch, and the data-parallel per-wave cost
+    (which only keeps data-parallel rows from biasing the others).  Also returns the mean and
+    the largest loss of picking the cheapest estimate among persistent / Stream-K / hybrid."""
+    import numpy as np
+    from scipy.optimize import nnls
+    rows = []
+    for shape, res in times.items():
+        M, N, K = map(int, shape.split("x"))
+        for tile, modes in res.items():
+            for mode, ms in modes.items():
+                rows.append((shape, tile, mode, ms * 1000.0, _features(M, N, K, tile, mode, sm_count)))
+    X = np.array([r[4] for r in rows])
+    y = np.array([r[3] for r in rows])
+    coef, _ = nnls(X / y[:, None], np.ones_like(y))
+    pred = X @ coef
+    losses = []
+    for shape in times:
+        rs = [(r, p) for r, p in zip(rows, pred) if r[0] == shape]
+        best = min(r[3] for r, _ in rs)
+        pick = min(((r, p) for r, p in rs if r[2] != "dp"), key=lambda t: t[1])[0]
+        losses.append(pick[3] / best - 1.0)
+    names = ["t_iter_pair", "t_iter_128x256", "t_iter_128x128", "t_piece", "t_split", "t_part",
+             "t_launch", "t_dp_wave"]
+    return dict(zip(names, (round(float(c), 4) for c in coef))), \
+        {"mean_loss": float(np.mean(losses)), "max_loss": float(np.max(losses))}

@@ -60,7 +60,7 @@ P = 0x100000  # a 16-byte aligned fake device address: never dereferenced by the
     dict(A=P + 8), dict(B=P + 2), dict(C=P + 4), dict(bias=P + 1),
     dict(M=0), dict(N=0), dict(K=0), dict(M=-5), dict(K=2 ** 31),
     dict(K=100), dict(N=100),            # bf16 needs 16-byte row pitches
-    dict(out_dtype=2), dict(mode=4), dict(mode=-1),
+    dict(out_dtype=2), dict(mode=5), dict(mode=-1),
 ])
 def test_bf16_bad_arguments_are_rejected_before_cuda(lib, args):
     a = dict(A=P, B=P, bias=None, C=P, out_dtype=1, M=64, N=64, K=64, num_sms=0, mode=2)
@@ -157,6 +157,27 @@ def test_plan_fields_follow_the_schedule_rules(lib):
     assert (p.tile_m, p.tile_n, p.tile_k, p.ctas_per_tile, p.grid) == (256, 256, 128, 2, 76)
     with pytest.raises(sk.SkError):
         sk.sk_plan(0, 0, 8, 8, 0, "dp", 148)
+
+
+def test_auto_mode_picks_a_concrete_plan_from_the_cost_model():
+    # choices of the fitted GB300 cost model on shapes of its calibration set (152 SMs)
+    cases = {(8192, 8192, 8192): (2, 2), (64, 14336, 4096): (1, 1), (512, 512, 32768): (1, 2),
+             (1536, 1536, 1536): (1, 1), (16384, 2048, 2048): (2, 1), (2304, 2304, 8192): (2, 2)}
+    for (M, N, K), (ctas_per_tile, mode) in cases.items():
+        p = sk.sk_plan(0, M, N, K, 0, "auto", 152)
+        assert (p.ctas_per_tile, p.mode) == (ctas_per_tile, mode), (M, N, K)
+        assert p.mode in (1, 2, 3)
+        rows = sk.sk_plan_segments(p)          # a concrete plan: its segments cover every tile
+        assert rows[:, 3].sum() - rows[:, 2].sum() == p.tiles * p.iters
+    # tiles the options force stay forced; MXFP4 never gets a 128x256 tile
+    p = sk.sk_plan(0, 8192, 8192, 8192, 0, "auto", 152, {"tile_m": 128, "tile_n": 128})
+    assert (p.tile_m, p.tile_n) == (128, 128)
+    for M in (256, 2048, 8192):
+        p = sk.sk_plan(1, M, 4096, 4096, 0, "auto", 152)
+        assert (p.ctas_per_tile, p.tile_n) in ((2, 256), (1, 128))
+    # one SM: no pairs, and still a plan
+    p = sk.sk_plan(0, 4096, 4096, 4096, 1, "auto", 152)
+    assert p.ctas_per_tile == 1 and p.grid == 1
 
 
 def test_pair_plans():
@@ -268,3 +289,16 @@ def test_streamk_256_cube_split_matches_golden(lib):
     plan = sk.sk_plan(0, 256, 256, 512, 3, "streamk", 148)
     got = sk.sk_plan_segments(plan)
     assert np.array_equal(got[:, :5], want)
+
+
+def test_auto_cost_constants_are_the_fit_of_the_shipped_sweep():
+    pytest.importorskip("scipy")
+    from sm_constrained_persistent_gb300 import tuning
+    coef, quality = tuning.fit(tuning.load())
+    src = open(os.path.join(ROOT, "sm_constrained_persistent_gb300", "csrc", "sk_api.cu")).read()
+    m = re.search(r"kCost = \{\{([^}]*)\}, ([^;]*)\};", src)
+    iters = [float(v) for v in m.group(1).split(",")]
+    rest = [float(v) for v in m.group(2).rstrip("}").split(",")]
+    assert iters == [coef["t_iter_pair"], coef["t_iter_128x256"], coef["t_iter_128x128"]]
+    assert rest == [coef["t_piece"], coef["t_split"], coef["t_part"], coef["t_launch"]]
+    assert quality["mean_loss"] < 0.02 and quality["max_loss"] < 0.15
