@@ -263,3 +263,25 @@ def test_4096_cube_num_sms_sweep_sampled():
 def test_skinny_64x14336x4096_num_sms_sweep_sampled():
     _sampled_check(inputs.workload("gemm_bf16_skinny_64x14336x4096"), "bf16",
                    ["dp", "persistent", "streamk", "hybrid"], (1, 16, 32, 64, 128, 0))
+
+
+# ---- matrices of at most 64 rows (one partly filled row of tiles) ---------------------------
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", [(1, 136, 512), (17, 1000, 1088), (64, 256, 4096),
+                                   (64, 14336, 256), (63, 8, 64)])
+@pytest.mark.parametrize("num_sms", [0, 5])
+def test_at_most_64_rows_integer_inputs_are_bit_exact(mode, shape, num_sms):
+    M, N, K = shape
+    p = inputs.bf16_problem(M, N, K, seed=M * 7 + N + K, integer=True, bias="f32_int")
+    c = gu.run_bf16(p, out="f32", mode=mode, num_sms=num_sms, options={"tile_n": 128})
+    want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), oracle.F32)
+    assert np.array_equal(gu.host_bits(c), want.view(np.uint32))
+
+
+def test_at_most_64_rows_random_bf16_output_matches_oracle():
+    p = inputs.bf16_problem(48, 2048, 8192, seed=12, operand_scale="sqrt_k", bias="bf16_uniform")
+    for mode in MODES:
+        c = gu.run_bf16(p, out="bf16", mode=mode)
+        ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "bf16")
+        gu.assert_close(gu.host_values(c), ref, "bf16", mode)
