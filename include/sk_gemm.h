@@ -132,6 +132,10 @@ sk_status_t sk_gemm_mxfp4(const void* A, const void* A_scale, const void* B,
  *                         pair) per 256 x 256 tile.  Pair tiles need tile_n 0 or 256 and at
  *                         least two SMs; num_sms then counts both SMs of every pair (an odd
  *                         num_sms leaves one SM unused).
+ *   hybrid_sk_waves:      SK_MODE_HYBRID only: full waves of g tiles added to the Stream-K
+ *                         region on top of the (tiles mod g) remainder (0 = the remainder only;
+ *                         1 = the "two-tile" variant, in which each CTA's Stream-K share is at
+ *                         least one whole tile).  Capped at the tiles there are.
  */
 typedef struct {
   int32_t tile_n;
@@ -140,7 +144,7 @@ typedef struct {
   int32_t inject_faults;
   int32_t drop_release_cta;
   int32_t tile_m;
-  int32_t reserved;
+  int32_t hybrid_sk_waves;
 } sk_options_t;
 
 sk_status_t sk_gemm_bf16_ex(const void* A, const void* B, const void* bias, void* C,

@@ -75,6 +75,8 @@ def _lib():
                                                   vp, i64, vp, i32]
             lib.oracle_schedule.restype = i64
             lib.oracle_schedule.argtypes = [i32, i64, i64, i64, vp, i64]
+            lib.oracle_schedule_hybrid.restype = i64
+            lib.oracle_schedule_hybrid.argtypes = [i32, i64, i64, i64, i64, vp, i64]
             lib.oracle_addmm_bf16_scheduled.restype = i32
             lib.oracle_addmm_bf16_scheduled.argtypes = [vp, vp, vp, i32, i64, i64, i64, i32,
                                                         i64, i64, i64, i64, vp]
@@ -293,14 +295,15 @@ def addmm_backward_bf16(dC, A, B, threads=0):
     return dA, dB, db
 
 
-def schedule(mode, tiles, iters, grid):
-    """List of (cta, tile, k_begin, k_end, role) segments, each CTA's in execution order."""
+def schedule(mode, tiles, iters, grid, hybrid_waves=0):
+    """List of (cta, tile, k_begin, k_end, role) segments, each CTA's in execution order.
+    hybrid_waves: full waves added to the hybrid's Stream-K region (the two-tile form)."""
     lib = _lib()
-    n = lib.oracle_schedule(mode, tiles, iters, grid, None, 0)
+    n = lib.oracle_schedule_hybrid(mode, tiles, iters, grid, hybrid_waves, None, 0)
     if n < 0:
         raise ValueError("bad schedule arguments")
     rows = np.zeros((max(n, 1), 5), dtype=np.int64)
-    lib.oracle_schedule(mode, tiles, iters, grid, _ptr(rows), n)
+    lib.oracle_schedule_hybrid(mode, tiles, iters, grid, hybrid_waves, _ptr(rows), n)
     return rows[:n]
 
 

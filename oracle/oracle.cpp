@@ -172,7 +172,11 @@ struct Segment {
 // A CTA runs, in order: the Stream-K tiles lying entirely in its range; its contribution
 // (the start of its range, if that is inside a tile); the tile its range ends in, if it owns
 // that tile but does not finish it; then its whole tiles outside the Stream-K region.
-std::vector<Segment> schedule(int mode, int64_t tiles, int64_t iters, int64_t grid) {
+// hybrid_waves: full waves of `grid` tiles added to the hybrid schedule's Stream-K region on
+// top of the (tiles mod grid) remainder -- the "two-tile" form of the hybrid, in which every
+// CTA's Stream-K share is at least one whole tile (0 = the remainder only).
+std::vector<Segment> schedule(int mode, int64_t tiles, int64_t iters, int64_t grid,
+                              int64_t hybrid_waves = 0) {
   std::vector<Segment> out;
   if (mode == MODE_DP) {
     for (int64_t t = 0; t < tiles; ++t) out.push_back({t, t, 0, iters, ROLE_FULL});
@@ -183,7 +187,9 @@ std::vector<Segment> schedule(int mode, int64_t tiles, int64_t iters, int64_t gr
       for (int64_t t = c; t < tiles; t += grid) out.push_back({c, t, 0, iters, ROLE_FULL});
     return out;
   }
-  const int64_t sk_tiles = (mode == MODE_STREAMK) ? tiles : tiles % grid;
+  const int64_t sk_tiles = (mode == MODE_STREAMK)
+                               ? tiles
+                               : std::min(tiles, tiles % grid + hybrid_waves * grid);
   const int64_t whole_tiles = tiles - sk_tiles;
   const int64_t total = sk_tiles * iters;
   const int64_t base = total / grid;
@@ -435,10 +441,10 @@ int oracle_addmm_mxfp4_at(const uint8_t* A, const uint8_t* A_scale, const uint8_
 // Writes up to `cap` rows of 5 int64 (cta, tile, k_begin, k_end, role) and returns the total
 // number of segments (call with cap = 0 to size the buffer).  role: 0 whole tile,
 // 1 owner of a split tile, 2 partial contribution.  Tiles are linear indices.
-int64_t oracle_schedule(int mode, int64_t tiles, int64_t iters, int64_t grid, int64_t* rows,
-                        int64_t cap) {
-  if (tiles < 1 || iters < 1 || grid < 1 || mode < 0 || mode > 3) return -1;
-  const std::vector<Segment> segs = schedule(mode, tiles, iters, grid);
+int64_t oracle_schedule_hybrid(int mode, int64_t tiles, int64_t iters, int64_t grid,
+                               int64_t hybrid_waves, int64_t* rows, int64_t cap) {
+  if (tiles < 1 || iters < 1 || grid < 1 || mode < 0 || mode > 3 || hybrid_waves < 0) return -1;
+  const std::vector<Segment> segs = schedule(mode, tiles, iters, grid, hybrid_waves);
   const int64_t n = static_cast<int64_t>(segs.size());
   for (int64_t i = 0; i < std::min(n, cap); ++i) {
     rows[5 * i + 0] = segs[i].cta;
@@ -448,6 +454,11 @@ int64_t oracle_schedule(int mode, int64_t tiles, int64_t iters, int64_t grid, in
     rows[5 * i + 4] = segs[i].role;
   }
   return n;
+}
+
+int64_t oracle_schedule(int mode, int64_t tiles, int64_t iters, int64_t grid, int64_t* rows,
+                        int64_t cap) {
+  return oracle_schedule_hybrid(mode, tiles, iters, grid, 0, rows, cap);
 }
 
 // Schedule-emulating bf16 addmm: for every tile, the partial sums of its segments (each a

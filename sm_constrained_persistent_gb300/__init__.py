@@ -36,7 +36,7 @@ class Options(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int32), ("raster_group", ctypes.c_int32),
                 ("spin_timeout_ns", ctypes.c_int64), ("inject_faults", ctypes.c_int32),
                 ("drop_release_cta", ctypes.c_int32), ("tile_m", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("hybrid_sk_waves", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):

@@ -99,7 +99,12 @@ sk_status_t make_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, 
     case SK_MODE_DP: grid = tiles; sk_tiles = 0; break;
     case SK_MODE_PERSISTENT: grid = std::min(units, tiles); sk_tiles = 0; break;
     case SK_MODE_STREAMK: grid = std::min(units, tiles * iters); sk_tiles = tiles; break;
-    default: grid = std::min(units, tiles * iters); sk_tiles = tiles % grid; break;
+    default: {
+      grid = std::min(units, tiles * iters);
+      const int64_t waves = opt != nullptr ? std::max<int32_t>(opt->hybrid_sk_waves, 0) : 0;
+      sk_tiles = std::min(tiles, tiles % grid + waves * grid);
+      break;
+    }
   }
   p->grid = static_cast<int32_t>(grid);
   p->whole_tiles = tiles - sk_tiles;
@@ -414,7 +419,8 @@ sk_status_t validate(int format, const void* A, const void* A_scale, const void*
     if (opt->tile_m != 0 && opt->tile_m != 128 && opt->tile_m != 256) return SK_ERR_INVALID_ARG;
     if (opt->tile_m == 256 && opt->tile_n == 128) return SK_ERR_INVALID_ARG;
     if (format == 1 && opt->tile_n == 256 && opt->tile_m != 256) return SK_ERR_INVALID_ARG;
-    if (opt->spin_timeout_ns < 0 || opt->raster_group < 0) return SK_ERR_INVALID_ARG;
+    if (opt->spin_timeout_ns < 0 || opt->raster_group < 0 || opt->hybrid_sk_waves < 0)
+      return SK_ERR_INVALID_ARG;
   }
   return SK_OK;
 }

@@ -133,6 +133,8 @@ def test_options_validation(lib):
                             {"spin_timeout_ns": -1}, None)
     assert st == sk.SK_ERR_INVALID_ARG
     assert sk.sk_workspace_reserve(0, None, 0) == sk.SK_ERR_INVALID_ARG
+    st = sk.sk_gemm_bf16_ex(P, P, None, P, 1, 64, 64, 64, 0, 3, {"hybrid_sk_waves": -1}, None)
+    assert st == sk.SK_ERR_INVALID_ARG
 
 
 # ---- planning -----------------------------------------------------------------------------
@@ -217,6 +219,18 @@ def test_pair_scheduler_matches_oracle_restatement(mode, shape, g):
     got = sk.sk_plan_segments(plan)
     want = oracle.schedule(sk.MODES[mode], plan.tiles, plan.iters, plan.grid)
     assert np.array_equal(got[:, :5], want)
+
+
+@pytest.mark.parametrize("shape", [(2304, 2304, 8192), (8192, 8192, 8192), (1000, 3000, 640)])
+@pytest.mark.parametrize("g", [7, 33, 0])
+@pytest.mark.parametrize("tile_m,waves", [(256, 1), (128, 1), (128, 2)])
+def test_two_tile_hybrid_matches_oracle_restatement(shape, g, tile_m, waves):
+    M, N, K = shape
+    plan = sk.sk_plan(0, M, N, K, g, "hybrid", 152, {"tile_m": tile_m, "hybrid_sk_waves": waves})
+    got = sk.sk_plan_segments(plan)
+    want = oracle.schedule(sk.MODES["hybrid"], plan.tiles, plan.iters, plan.grid, waves)
+    assert np.array_equal(got[:, :5], want)
+    assert plan.sk_tiles == min(plan.tiles, plan.tiles % plan.grid + waves * plan.grid)
 
 
 def _same_split(mode, M, N, K, g_req, sms, tile_n):

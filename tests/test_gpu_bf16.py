@@ -285,3 +285,17 @@ def test_at_most_64_rows_random_bf16_output_matches_oracle():
         c = gu.run_bf16(p, out="bf16", mode=mode)
         ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "bf16")
         gu.assert_close(gu.host_values(c), ref, "bf16", mode)
+
+
+# ---- the two-tile hybrid (full waves added to the Stream-K region) --------------------------
+
+@pytest.mark.parametrize("shape", [(2304, 2304, 1024), (1000, 3000, 640), (520, 776, 1000)])
+@pytest.mark.parametrize("tile", ["128x128", "pair256"])
+@pytest.mark.parametrize("num_sms,waves", [(0, 1), (14, 1), (14, 2)])
+def test_two_tile_hybrid_integer_inputs_are_bit_exact(shape, tile, num_sms, waves):
+    M, N, K = shape
+    p = inputs.bf16_problem(M, N, K, seed=M + N + waves, integer=True, bias="f32_int")
+    c = gu.run_bf16(p, out="f32", mode="hybrid", num_sms=num_sms,
+                    options=dict(TILES[tile], hybrid_sk_waves=waves))
+    want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), oracle.F32)
+    assert np.array_equal(gu.host_bits(c), want.view(np.uint32))

@@ -355,9 +355,10 @@ def test_mxfp4_sampled_elements_agree_with_full():
 # schedules
 # ---------------------------------------------------------------------------------------
 
-def _check_schedule(mode, T, I, g):
-    segs = oracle.schedule(mode, T, I, g)
-    whole = {oracle.MODE_STREAMK: 0, oracle.MODE_HYBRID: T - T % g}.get(mode, T)
+def _check_schedule(mode, T, I, g, hybrid_waves=0):
+    segs = oracle.schedule(mode, T, I, g, hybrid_waves)
+    whole = {oracle.MODE_STREAMK: 0,
+             oracle.MODE_HYBRID: T - min(T, T % g + hybrid_waves * g)}.get(mode, T)
     cover = np.zeros((T, I), dtype=np.int64)
     owners = {}
     per_cta = {}
@@ -420,6 +421,31 @@ def test_streamk_and_hybrid_schedule_invariants(T, I, g):
         whole = [t for t, k0, k1, r in lst if t < T - sk_tiles]
         assert whole == list(range(cta, T - sk_tiles, g_sk))
         assert all(k0 == 0 and k1 == I for t, k0, k1, r in lst if t < T - sk_tiles)
+
+
+@pytest.mark.parametrize("T,I", [(81, 128), (225, 16), (13, 64), (1024, 32), (7, 3)])
+@pytest.mark.parametrize("g", [2, 5, 76, 152])
+@pytest.mark.parametrize("waves", [1, 2])
+def test_two_tile_hybrid_schedule(T, I, g, waves):
+    # the hybrid with `waves` full waves added to its Stream-K region: the same invariants,
+    # and every CTA's Stream-K share is at least `waves` whole tiles' worth when the tiles
+    # allow it
+    g = min(g, T * I)
+    segs, per_cta = _check_schedule(oracle.MODE_HYBRID, T, I, g, waves)
+    sk_tiles = min(T, T % g + waves * g)
+    sk_iters = [sum(k1 - k0 for t, k0, k1, _ in per_cta.get(c, []) if t >= T - sk_tiles)
+                for c in range(g)]
+    assert sum(sk_iters) == sk_tiles * I
+    if sk_tiles < T:
+        assert min(sk_iters) >= waves * I
+    for cta, lst in per_cta.items():
+        whole = [t for t, k0, k1, r in lst if t < T - sk_tiles]
+        assert whole == list(range(cta, T - sk_tiles, g))
+    # waves = 0 is the plain hybrid; enough waves make it Stream-K over every tile
+    assert np.array_equal(oracle.schedule(oracle.MODE_HYBRID, T, I, g, 0),
+                          oracle.schedule(oracle.MODE_HYBRID, T, I, g))
+    assert np.array_equal(oracle.schedule(oracle.MODE_HYBRID, T, I, g, T),
+                          oracle.schedule(oracle.MODE_STREAMK, T, I, g))
 
 
 @pytest.mark.parametrize("T,g", [(1, 1), (10, 3), (1024, 148), (225, 152), (5, 9)])
