@@ -110,9 +110,10 @@ def measured_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-# Sources that take no part in the launches the traffic figures were captured from (the
-# host-buffer copies, the no-allocation entry point, the backward's column sum).
-NOT_IN_CAPTURED_LAUNCHES = {"sk_host.cu", "sk_static.cu", "sk_reduce.cu"}
+# Sources outside the captured kernels' device code: the host API (its planning is checked
+# separately, by comparing the recorded plan), the host-buffer copies, the no-allocation entry
+# point and the backward's column sum.
+NOT_IN_CAPTURED_LAUNCHES = {"sk_api.cu", "sk_host.cu", "sk_static.cu", "sk_reduce.cu"}
 
 
 def kernel_source_hash():
@@ -127,8 +128,16 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_key):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+def plan_signature(plan):
+    """The launch a plan makes: grid, CTAs per tile, tile and the Stream-K split."""
+    return {"grid": plan.grid, "ctas_per_tile": plan.ctas_per_tile,
+            "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "sk_tiles": plan.sk_tiles,
+            "whole_tiles": plan.whole_tiles, "raster_group": plan.raster_group}
+
+
+def recorded_traffic(kernel_key, plan=None):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel
+    source and (when recorded) the same launch plan."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -137,7 +146,11 @@ def recorded_traffic(kernel_key):
     if d.get("kernel_source_hash") != kernel_source_hash():
         return None
     entry = d.get("kernels", {}).get(kernel_key)
-    return None if entry is None else entry.get("dram_bytes_per_launch")
+    if entry is None:
+        return None
+    if plan is not None and "plan" in entry and entry["plan"] != plan_signature(plan):
+        return None
+    return entry.get("dram_bytes_per_launch")
 
 
 class ClockSampler:
@@ -477,14 +490,14 @@ def run_ours(args):
         achieved = alg_bytes / (gemm_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": round(hbm, 1),
                     "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                    "traffic": recorded_traffic(kernel_key),
+                    "traffic": recorded_traffic(kernel_key, plan),
                     "peak_source": f"copy bandwidth, {peak_src}", "kernel": kernel_key,
                     "algorithmic_bytes": alg_bytes}
     else:
         achieved = prob.flops / (gemm_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                    "traffic": recorded_traffic(kernel_key), "peak_source": peak_note,
+                    "traffic": recorded_traffic(kernel_key, plan), "peak_source": peak_note,
                     "kernel": kernel_key, "algorithmic_flops": prob.flops}
 
     e2e = None
