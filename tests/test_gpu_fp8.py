@@ -134,3 +134,25 @@ def test_addmm_fp8_8192_cube_sampled():
         got = c.float()[torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda()]
         gu.assert_close(got.cpu().numpy().astype(np.float64), ref, "bf16", mode)
         del c
+
+
+def test_cuda_graph_replay_of_an_fp8_streamk_call():
+    M, N, K = 768, 512, 2048
+    s = torch.cuda.Stream()
+    a = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    b = torch.empty((K, N), dtype=torch.uint8, device="cuda")
+    c = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    assert sk.sk_workspace_reserve(0, s.cuda_stream, 152) == sk.SK_OK
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        sk.gemm_fp8(a, b, None, out=c, mode="streamk", stream=s)
+    for seed in (1, 2):
+        p = inputs.fp8_problem(M, N, K, seed=seed, integer=True)
+        a.copy_(gu.dev_u8(p["A"]))
+        b.copy_(gu.dev_u8(p["B"]))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert sk.sk_stream_status(s.cuda_stream) == sk.SK_OK
+        assert np.array_equal(gu.host_bits(c), _want_bits(p, "f32"))

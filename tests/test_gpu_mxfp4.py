@@ -103,3 +103,30 @@ def test_addmm_mxfp4_8192_cube_sampled():
         sk.stream_status()
         got = c.float()[torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda()]
         gu.assert_close(got.cpu().numpy().astype(np.float64), ref, "bf16", mode)
+
+
+def test_cuda_graph_replay_of_an_mxfp4_streamk_call():
+    # the scale re-layout buffer and the Stream-K slots are reserved before capture
+    M, N, K = 768, 512, 2048
+    s = torch.cuda.Stream()
+    a = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    b = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+    asc = torch.empty((M, K // 32), dtype=torch.uint8, device="cuda")
+    bsc = torch.empty((N, K // 32), dtype=torch.uint8, device="cuda")
+    c = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    assert sk.sk_workspace_reserve(0, s.cuda_stream, 152, M, N, K) == sk.SK_OK
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        sk.gemm_mxfp4(a, asc, b, bsc, None, out=c, mode="streamk", stream=s)
+    for seed in (1, 2):
+        p = inputs.mxfp4_problem(M, N, K, seed=seed, exp_range=1)
+        for dst, src in ((a, "A"), (b, "B"), (asc, "A_scale"), (bsc, "B_scale")):
+            dst.copy_(gu.dev_u8(p[src]))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert sk.sk_stream_status(s.cuda_stream) == sk.SK_OK
+        want = oracle.round_output(
+            oracle.addmm_mxfp4(p["A"], p["A_scale"], p["B"], p["B_scale"], None), oracle.F32)
+        assert np.array_equal(gu.host_bits(c), want.view(np.uint32))
