@@ -678,9 +678,16 @@ def auto_selection(device, sm_count, bpeak, dist):
                                        bpeak, dist, options=opt).items():
                 if best is None or r["ms"] < best["ms"]:
                     best = dict(r, mode=mode)
+        # the measured choice: sk_autotune on this problem, then auto mode again
+        import sm_constrained_persistent_gb300 as sk
+        d = pr.dev
+        sk.autotune("bf16", d["A"], d["B"], d.get("bias"), out=pr.C, reps=5)
+        tuned = _time_modes(pr, ["auto"], sm_count, bpeak, dist)["auto"]
         res[name] = {"auto_ms": auto["ms"], "auto_tile": auto["tile"], "best_ms": best["ms"],
                      "best": f"{best['mode']} {best['tile']}",
-                     "auto_over_best": round(auto["ms"] / best["ms"], 3)}
+                     "auto_over_best": round(auto["ms"] / best["ms"], 3),
+                     "autotuned_ms": tuned["ms"],
+                     "autotuned_over_best": round(tuned["ms"] / best["ms"], 3)}
         del pr
     return res
 

@@ -319,6 +319,26 @@ sk_status_t sk_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, sk
                     int sm_count, const sk_options_t* options, sk_plan_t* plan);
 
 /*
+ * sk_autotune — measure every schedule x tile candidate for one problem on `stream` and keep
+ * the fastest: later SK_MODE_AUTO calls with the same device, format, output dtype, M, N, K
+ * and num_sms (and no forced tile in their options) use it instead of the cost model.  This is
+ * the measured form of the optional tuning step of the SM-constraint GEMM page (flashinfer PR
+ * #982, "tune: get best config for gemm").
+ *   Operands, C and the other arguments as the format's _ex call (format 0 bf16, 1 MXFP4,
+ *   2 fp8; plain layouts).  Each candidate runs once to warm up, then `reps` times (1..1000)
+ *   between two events; C holds the product afterwards (from the last candidate run).
+ *   chosen (may be NULL) receives the winning plan (its `mode` field is the schedule);
+ *   best_ms (may be NULL) its mean time per call in milliseconds.
+ *   Synchronises `stream`; refused (SK_ERR_UNSUPPORTED) while `stream` is being captured.
+ *   Kernel errors during the runs are returned as by sk_stream_status.  The measured choices
+ *   are kept until sk_workspace_release_all.
+ */
+sk_status_t sk_autotune(int format, const void* A, const void* A_scale, const void* B,
+                        const void* B_scale, const void* bias, void* C, sk_dtype_t out_dtype,
+                        int64_t M, int64_t N, int64_t K, int num_sms, int reps, sk_plan_t* chosen,
+                        float* best_ms, void* stream);
+
+/*
  * Enumerates the work the kernel's CTAs (or CTA pairs) perform for `plan`, in each one's
  * execution order: rows of 7 int64 (unit, linear tile, k_begin, k_end, role, tile_m index,
  * tile_n index), role

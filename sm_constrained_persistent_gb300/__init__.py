@@ -112,6 +112,9 @@ def lib():
             h.sk_plan.restype = i32
             h.sk_plan.argtypes = [i32, i64, i64, i64, i32, i32, i32, ctypes.POINTER(Options),
                                   ctypes.POINTER(Plan)]
+            h.sk_autotune.restype = i32
+            h.sk_autotune.argtypes = [i32, vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, i32, i32,
+                                      ctypes.POINTER(Plan), ctypes.POINTER(ctypes.c_float), vp]
             h.sk_device_caps.restype = i32
             h.sk_device_caps.argtypes = [i32, ctypes.POINTER(DeviceCaps)]
             h.sk_plan_segments.restype = i64
@@ -406,6 +409,29 @@ def addmm_backward(dc, a, b, need=("a", "b", "bias"), grad_dtype=None, num_sms=0
                                 num_sms, _mode(mode), _stream_ptr(stream))
     _check(st, "sk_addmm_backward_bf16")
     return da, db, dbias
+
+
+def autotune(fmt, a, b, bias=None, out=None, out_dtype=None, a_scale=None, b_scale=None,
+             num_sms=0, reps=5, stream=None):
+    """Measure every schedule x tile candidate for this problem on the GPU and keep the fastest
+    for later mode="auto" calls.  CUDA tensors as for gemm_bf16 / gemm_fp8 / gemm_mxfp4.
+    Returns (plan, ms per call)."""
+    import torch
+    if fmt == "mxfp4":
+        M, K, N = a.shape[0], a.shape[1] * 2, b.shape[0]
+    else:
+        (M, K), N = a.shape, b.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=a.device)
+    od = SK_BF16 if out.dtype == torch.bfloat16 else SK_F32
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    plan, ms = Plan(), ctypes.c_float()
+    st = lib().sk_autotune({"bf16": 0, "mxfp4": 1, "fp8": 2}[fmt], a.data_ptr(), ptr(a_scale),
+                           b.data_ptr(), ptr(b_scale), ptr(bias), out.data_ptr(), od, M, N, K,
+                           num_sms, reps, ctypes.byref(plan), ctypes.byref(ms),
+                           _stream_ptr(stream))
+    _check(st, "sk_autotune")
+    return plan, ms.value
 
 
 def stream_status(stream=None):

@@ -243,6 +243,26 @@ std::mutex g_mutex;
 std::map<int, DeviceInfo> g_devices;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
 
+// Choices measured by sk_autotune, per device and problem; SK_MODE_AUTO uses them first.
+struct TuneKey {
+  int dev, format, layout, out_dtype, num_sms;
+  int64_t M, N, K;
+  bool operator<(const TuneKey& o) const {
+    if (dev != o.dev) return dev < o.dev;
+    if (format != o.format) return format < o.format;
+    if (layout != o.layout) return layout < o.layout;
+    if (out_dtype != o.out_dtype) return out_dtype < o.out_dtype;
+    if (num_sms != o.num_sms) return num_sms < o.num_sms;
+    if (M != o.M) return M < o.M;
+    if (N != o.N) return N < o.N;
+    return K < o.K;
+  }
+};
+struct TuneChoice {
+  int mode, tile_m, tile_n, hybrid_sk_waves;
+};
+std::map<TuneKey, TuneChoice> g_tuned;   // guarded by g_mutex
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -441,6 +461,26 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   DeviceInfo* di = nullptr;
   if ((st = device_info(dev, &di)) != SK_OK) return st;
   if (di->cc_major != 10 || di->cc_minor != 3) return SK_ERR_UNSUPPORTED;   // built for sm_103a
+
+  // SK_MODE_AUTO: a choice measured by sk_autotune for this problem wins over the cost model
+  // (when the options force no tile).
+  sk_options_t tuned_opt = {};
+  if (mode == SK_MODE_AUTO && (opt == nullptr || (opt->tile_m == 0 && opt->tile_n == 0))) {
+    const auto it = g_tuned.find(TuneKey{dev, format, layout, static_cast<int>(out_dtype),
+                                         num_sms <= 0 ? 0 : num_sms, M, N, K});
+    if (it != g_tuned.end()) {
+      if (opt != nullptr) {
+        tuned_opt = *opt;
+      } else {
+        tuned_opt.drop_release_cta = -1;
+      }
+      tuned_opt.tile_m = it->second.tile_m;
+      tuned_opt.tile_n = it->second.tile_n;
+      tuned_opt.hybrid_sk_waves = it->second.hybrid_sk_waves;
+      opt = &tuned_opt;
+      mode = static_cast<sk_mode_t>(it->second.mode);
+    }
+  }
 
   // The pair variants' cluster capacity is needed to plan; set both candidates up first.
   const int pair_variant = format == 1   ? sk::kVariantMxPair
@@ -727,6 +767,7 @@ void sk_workspace_release_all(void) {
     if (w.red) cudaFree(w.red);
   }
   g_workspaces.clear();
+  g_tuned.clear();
   cudaSetDevice(prev);
   sk::release_host_stages();
 }
@@ -777,6 +818,104 @@ sk_status_t sk_device_caps(int device, sk_device_caps_t* caps) {
   }
   cudaSetDevice(prev);
   return st;
+}
+
+sk_status_t sk_autotune(int format, const void* A, const void* A_scale, const void* B,
+                        const void* B_scale, const void* bias, void* C, sk_dtype_t out_dtype,
+                        int64_t M, int64_t N, int64_t K, int num_sms, int reps, sk_plan_t* chosen,
+                        float* best_ms, void* stream_ptr) {
+  if (format < 0 || format > 2 || reps < 1 || reps > 1000) return SK_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return SK_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return SK_ERR_UNSUPPORTED;   // timing synchronises
+  int dev = 0, sm_count = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SK_ERR_UNSUPPORTED;
+  struct Cand {
+    int tile_m, tile_n, mode, waves;
+  };
+  const Cand cands[] = {
+      {256, 256, SK_MODE_PERSISTENT, 0}, {256, 256, SK_MODE_STREAMK, 0},
+      {256, 256, SK_MODE_HYBRID, 0},     {256, 256, SK_MODE_HYBRID, 1},
+      {128, 256, SK_MODE_PERSISTENT, 0}, {128, 256, SK_MODE_STREAMK, 0},
+      {128, 256, SK_MODE_HYBRID, 0},     {128, 128, SK_MODE_PERSISTENT, 0},
+      {128, 128, SK_MODE_STREAMK, 0},    {128, 128, SK_MODE_HYBRID, 0},
+      {128, 128, SK_MODE_HYBRID, 1}};
+  auto run = [&](const Cand& c) -> sk_status_t {
+    sk_options_t o = {};
+    o.drop_release_cta = -1;
+    o.tile_m = c.tile_m;
+    o.tile_n = c.tile_n;
+    o.hybrid_sk_waves = c.waves;
+    const sk_mode_t m = static_cast<sk_mode_t>(c.mode);
+    switch (format) {
+      case 0: return sk_gemm_bf16_ex(A, B, bias, C, out_dtype, M, N, K, num_sms, m, &o, stream);
+      case 2: return sk_gemm_fp8_ex(A, B, bias, C, out_dtype, M, N, K, num_sms, m, &o, stream);
+      default:
+        return sk_gemm_mxfp4_ex(A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sms, m,
+                                &o, stream);
+    }
+  };
+  cudaEvent_t ev[2];
+  if (cudaEventCreate(&ev[0]) != cudaSuccess) return SK_ERR_CUDA;
+  if (cudaEventCreate(&ev[1]) != cudaSuccess) {
+    cudaEventDestroy(ev[0]);
+    return SK_ERR_CUDA;
+  }
+  sk_status_t result = SK_ERR_INVALID_ARG;   // no candidate ran
+  float best = 0.0f;
+  const Cand* pick = nullptr;
+  for (const Cand& c : cands) {
+    sk_status_t st = run(c);                       // warm-up; refuses invalid combinations
+    if (st == SK_ERR_INVALID_ARG || st == SK_ERR_NOT_CORESIDENT) continue;
+    if (st != SK_OK) {
+      result = st;
+      pick = nullptr;
+      break;
+    }
+    cudaEventRecord(ev[0], stream);
+    for (int r = 0; r < reps && st == SK_OK; ++r) st = run(c);
+    cudaEventRecord(ev[1], stream);
+    if (st == SK_OK) st = sk_stream_status(stream);   // synchronises; reports kernel errors
+    if (st != SK_OK) {
+      result = st;
+      pick = nullptr;
+      break;
+    }
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, ev[0], ev[1]) != cudaSuccess) {
+      result = SK_ERR_CUDA;
+      pick = nullptr;
+      break;
+    }
+    ms /= static_cast<float>(reps);
+    if (pick == nullptr || ms < best) {
+      best = ms;
+      pick = &c;
+    }
+    result = SK_OK;
+  }
+  cudaEventDestroy(ev[0]);
+  cudaEventDestroy(ev[1]);
+  if (result != SK_OK || pick == nullptr) return result;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_tuned[TuneKey{dev, format, 0, static_cast<int>(out_dtype), num_sms <= 0 ? 0 : num_sms, M,
+                    N, K}] = TuneChoice{pick->mode, pick->tile_m, pick->tile_n, pick->waves};
+  }
+  if (best_ms != nullptr) *best_ms = best;
+  if (chosen != nullptr) {
+    sk_options_t o = {};
+    o.drop_release_cta = -1;
+    o.tile_m = pick->tile_m;
+    o.tile_n = pick->tile_n;
+    o.hybrid_sk_waves = pick->waves;
+    return sk_plan(format, M, N, K, num_sms, static_cast<sk_mode_t>(pick->mode), sm_count, &o,
+                   chosen);
+  }
+  return SK_OK;
 }
 
 sk_status_t sk_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, sk_mode_t mode,

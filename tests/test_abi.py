@@ -37,7 +37,8 @@ def test_header_declares_the_boundary():
     for required in ["sk_gemm_bf16", "sk_gemm_mxfp4", "sk_stream_status", "sk_workspace_reserve",
                      "sk_workspace_release_all", "sk_status_string", "sk_plan", "sk_plan_segments",
                      "sk_gemm_bf16_ex", "sk_gemm_mxfp4_ex", "sk_gemm_fp8", "sk_gemm_fp8_ex",
-                     "sk_gemm_bf16_host", "sk_gemm_fp8_host", "sk_gemm_mxfp4_host"]:
+                     "sk_gemm_bf16_host", "sk_gemm_fp8_host", "sk_gemm_mxfp4_host",
+                     "sk_autotune"]:
         assert required in names
 
 

@@ -53,3 +53,40 @@ def test_backward_and_host_calls_accept_auto():
                         mode="auto", out_dtype=torch.float32)
     want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], None), oracle.F32)
     assert np.array_equal(host.numpy().view(np.uint32), want.view(np.uint32))
+
+
+def test_autotune_picks_a_measured_plan_that_auto_mode_then_uses():
+    p = inputs.bf16_problem(1536, 1024, 2048, seed=21, operand_scale="sqrt_k", bias="f32_normal")
+    a, b, bias = gu.dev_bf16(p["A"]), gu.dev_bf16(p["B"]), gu.dev_bias(p["bias"])
+    plan, ms = sk.autotune("bf16", a, b, bias, out_dtype=torch.float32, reps=3)
+    assert plan.mode in (1, 2, 3) and ms > 0
+    ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "f32")
+    auto = sk.gemm_bf16(a, b, bias, out_dtype=torch.float32, mode="auto")
+    sk.stream_status()
+    gu.assert_close(gu.host_values(auto), ref, "f32")
+    # the same plan run explicitly gives the same bits: auto used the measured choice
+    opts = {"tile_m": plan.tile_m, "tile_n": plan.tile_n,
+            "hybrid_sk_waves": 1 if (plan.mode == 3 and plan.sk_tiles > plan.tiles % plan.grid) else 0}
+    explicit = sk.gemm_bf16(a, b, bias, out_dtype=torch.float32, mode=int(plan.mode), options=opts)
+    sk.stream_status()
+    assert torch.equal(auto, explicit)
+
+
+def test_autotune_fp8_and_mxfp4():
+    p = inputs.fp8_problem(1024, 768, 1024, seed=22, integer=True)
+    a, b = gu.dev_u8(p["A"]), gu.dev_u8(p["B"])
+    plan, ms = sk.autotune("fp8", a, b, out_dtype=torch.float32, reps=2)
+    c = sk.gemm_fp8(a, b, out_dtype=torch.float32, mode="auto")
+    sk.stream_status()
+    want = oracle.round_output(oracle.addmm_fp8(p["A"], p["B"], None), oracle.F32)
+    assert np.array_equal(gu.host_bits(c), want.view(np.uint32))
+    q = inputs.mxfp4_problem(512, 768, 1024, seed=23, exp_range=1)
+    args = [gu.dev_u8(q[k]) for k in ("A", "A_scale", "B", "B_scale")]
+    plan, ms = sk.autotune("mxfp4", args[0], args[2], a_scale=args[1], b_scale=args[3],
+                           out_dtype=torch.float32, reps=2)
+    assert plan.tile_n in (128, 256) and ms > 0
+    c = sk.gemm_mxfp4(*args, None, out_dtype=torch.float32, mode="auto")
+    sk.stream_status()
+    want = oracle.round_output(oracle.addmm_mxfp4(q["A"], q["A_scale"], q["B"], q["B_scale"], None),
+                               oracle.F32)
+    assert np.array_equal(gu.host_bits(c), want.view(np.uint32))
