@@ -334,7 +334,7 @@ def needs_flush(prob):
     return operand_bytes < L2_FLUSH_BYTES
 
 
-def time_calls(prob, mode, num_sms, steps, warmup, dist=None, options=None):
+def time_calls(prob, mode, num_sms, steps, warmup, dist=None, options=None, flush=None):
     """Device time of `steps` calls (after `warmup`), CUDA events on the launch stream,
     barrier + synchronize on both sides.  Back to back when the operands exceed L2; otherwise
     a 256 MiB write flushes L2 before each call and only the calls are timed.
@@ -343,7 +343,7 @@ def time_calls(prob, mode, num_sms, steps, warmup, dist=None, options=None):
     import sm_constrained_persistent_gb300 as sk
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
-    flush = needs_flush(prob)
+    flush = needs_flush(prob) if flush is None else flush
     scrub = L2Flush(prob.device) if flush else None
     for _ in range(warmup):
         st = prob.call(mode, num_sms, sp, options=options)
@@ -541,12 +541,13 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def _time_modes(pr, modes, sm_count, peak, dist, num_sms=0, options=None, steps=10, warmup=3):
+def _time_modes(pr, modes, sm_count, peak, dist, num_sms=0, options=None, steps=10, warmup=3,
+                flush=None):
     """ms, TFLOPS, % of peak, grid, tile and tile-quantisation efficiency per mode."""
     import sm_constrained_persistent_gb300 as sk
     res = {}
     for mode in modes:
-        total, _ = time_calls(pr, mode, num_sms, steps, warmup, dist, options)
+        total, _ = time_calls(pr, mode, num_sms, steps, warmup, dist, options, flush)
         ms = total / steps
         plan = sk.sk_plan(FORMAT_CODE[pr.fmt], pr.M, pr.N, pr.K, num_sms, mode, sm_count,
                           options)
@@ -735,6 +736,16 @@ def extras(prob, sm_count, dist):
             rows[str(ns)] = r
         sweep[name] = rows
     out["num_sms_sweep_persistent"] = sweep
+    # warm L2 (operands left in L2 by the previous call) against the flushed numbers above
+    warm = {}
+    for name, opt in [("gemm_bf16_1920x1920x16384", {"tile_m": 128, "tile_n": 128}),
+                      ("gemm_bf16_skinny_64x14336x4096", None)]:
+        pr = get(name)
+        cold = _time_modes(pr, ["persistent", "streamk"], sm_count, bpeak, dist, options=opt)
+        hot = _time_modes(pr, ["persistent", "streamk"], sm_count, bpeak, dist, options=opt,
+                          flush=False)
+        warm[name] = {m: {"cold_ms": cold[m]["ms"], "warm_ms": hot[m]["ms"]} for m in cold}
+    out["l2_warm_vs_cold"] = warm
     out["auto_selection"] = auto_selection(prob.device, sm_count, bpeak, dist)
     out["corun_half_sms"] = corun(get("addmm_bf16_8192"), sm_count)
     out["addmm_backward_bf16_8192"] = backward(get("addmm_bf16_8192"), bpeak)
