@@ -150,6 +150,23 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch,
   }
 }
 
+// Eight float4 of one Stream-K partial (one 32-column chunk of a row), `stride` float4 apart.
+__device__ __forceinline__ void load_partial8(float4 (&b)[8], const float4* src, int stride) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) b[q] = __ldcg(src + q * stride);
+}
+
+// sum = b (first) or sum += b, for one 32-column chunk.
+__device__ __forceinline__ void add_partial8(float (&sum)[32], const float4 (&b)[8], bool first) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    sum[4 * q] = first ? b[q].x : sum[4 * q] + b[q].x;
+    sum[4 * q + 1] = first ? b[q].y : sum[4 * q + 1] + b[q].y;
+    sum[4 * q + 2] = first ? b[q].z : sum[4 * q + 2] + b[q].z;
+    sum[4 * q + 3] = first ? b[q].w : sum[4 * q + 3] + b[q].w;
+  }
+}
+
 // Adds bias[n0 .. n0+32) (those below N) to v.
 __device__ __forceinline__ void add_bias_chunk(const Args& a, int64_t n0, float (&v)[32]) {
   if (a.bias == nullptr) return;
@@ -593,27 +610,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float4* src0 = reinterpret_cast<const float4*>(args.P + (cta + 1) * (kBM * kBN)) +
                                  static_cast<int64_t>(ch) * 8 * kBM + row;
             float sum[32];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 p = __ldcg(src0 + q * kBM);
-              sum[4 * q] = p.x;
-              sum[4 * q + 1] = p.y;
-              sum[4 * q + 2] = p.z;
-              sum[4 * q + 3] = p.w;
-            }
+            float4 pp[8];
+            load_partial8(pp, src0, kBM);
+            add_partial8(sum, pp, true);
 #pragma unroll 1
             for (int c = 1; c < n_contrib; ++c) {
-              const float4* src = src0 + static_cast<int64_t>(c) * (kBM * kBN / 4);
-              float4 p[8];
-#pragma unroll
-              for (int q = 0; q < 8; ++q) p[q] = __ldcg(src + q * kBM);
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                sum[4 * q] += p[q].x;
-                sum[4 * q + 1] += p[q].y;
-                sum[4 * q + 2] += p[q].z;
-                sum[4 * q + 3] += p[q].w;
-              }
+              load_partial8(pp, src0 + static_cast<int64_t>(c) * (kBM * kBN / 4), kBM);
+              add_partial8(sum, pp, false);
             }
             __syncwarp();
             tmem_store_32cols(t_stage + ch * 32, sum);

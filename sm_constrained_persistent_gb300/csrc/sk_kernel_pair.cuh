@@ -502,27 +502,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
                 reinterpret_cast<const float4*>(args.P + (2 * (pair + 1) + rank) * (kBM * kBN)) +
                 static_cast<int64_t>(half * 4 + ch) * 8 * kBM + row;
             float sum[32];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 p = __ldcg(src0 + q * kBM);
-              sum[4 * q] = p.x;
-              sum[4 * q + 1] = p.y;
-              sum[4 * q + 2] = p.z;
-              sum[4 * q + 3] = p.w;
-            }
+            float4 pp[8];
+            load_partial8(pp, src0, kBM);
+            add_partial8(sum, pp, true);
 #pragma unroll 1
             for (int c = 1; c < n_contrib; ++c) {
-              const float4* src = src0 + static_cast<int64_t>(2 * c) * (kBM * kBN / 4);
-              float4 p[8];
-#pragma unroll
-              for (int q = 0; q < 8; ++q) p[q] = __ldcg(src + q * kBM);
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                sum[4 * q] += p[q].x;
-                sum[4 * q + 1] += p[q].y;
-                sum[4 * q + 2] += p[q].z;
-                sum[4 * q + 3] += p[q].w;
-              }
+              load_partial8(pp, src0 + static_cast<int64_t>(2 * c) * (kBM * kBN / 4), kBM);
+              add_partial8(sum, pp, false);
             }
             __syncwarp();
             tmem_store_32cols(t_stage + ch * 32, sum);
@@ -584,53 +570,99 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
         break;   // the last piece
       }
 
-      // Drain this thread's 128 columns, then hand the accumulator back.
-      float v[128];
-      __syncwarp();
-      tmem_load_64cols(t_row, reinterpret_cast<uint32_t*>(v));
-      tmem_load_64cols(t_row + 64, reinterpret_cast<uint32_t*>(v) + 64);
-      tmem_load_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) remote_arrive(tempty_leader0 + acc * 8);
-
-      if (u.role == kRoleContrib) {
-        float4* dst = reinterpret_cast<float4*>(args.P + cta * (kBM * kBN)) +
-                      static_cast<int64_t>(half * 4) * 8 * kBM + row;
+      if constexpr (Cf::kAccBufs == 2) {
+        // Two accumulators: the MMA works on the other one meanwhile, so this one is drained
+        // and stored 32 columns at a time and handed back at the end.
+        float4* my_slot = reinterpret_cast<float4*>(args.P + cta * (kBM * kBN)) +
+                          static_cast<int64_t>(half * 4) * 8 * kBM + row;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_load_32cols(t_row + ch * 32, r);
+          tmem_load_wait();
+          float w[32];
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          __stcg(dst + q * kBM, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
-        __threadfence();
-        named_barrier_sync(1, kPairEpilogueThreads);
-        if (et == 0 && !(args.inject_drop && cta == args.drop_cta))
-          flag_release(args.flags + cta, args.epoch);
-      } else if (status == kUnitStore) {
-        for (int c = 0; c < n_contrib; ++c) {
-          const float4* src =
-              reinterpret_cast<const float4*>(args.P + (2 * (pair + 1 + c) + rank) * (kBM * kBN)) +
-              static_cast<int64_t>(half * 4) * 8 * kBM + row;
+          for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(r[j]);
+          if (u.role == kRoleContrib) {
+            float4* dst = my_slot + static_cast<int64_t>(ch) * 8 * kBM;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            float4 p[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) p[q] = __ldcg(src + (ch * 8 + q) * kBM);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              v[ch * 32 + 4 * q] += p[q].x;
-              v[ch * 32 + 4 * q + 1] += p[q].y;
-              v[ch * 32 + 4 * q + 2] += p[q].z;
-              v[ch * 32 + 4 * q + 3] += p[q].w;
+            for (int q = 0; q < 8; ++q)
+              __stcg(dst + q * kBM, make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
+          } else if (status == kUnitStore) {
+            for (int c = 0; c < n_contrib; ++c) {
+              const float4* src =
+                  reinterpret_cast<const float4*>(args.P + (2 * (pair + 1 + c) + rank) * (kBM * kBN)) +
+                  static_cast<int64_t>(half * 4 + ch) * 8 * kBM + row;
+              float4 pp[8];
+              load_partial8(pp, src, kBM);
+              add_partial8(w, pp, false);
             }
-            asm volatile("" ::: "memory");   // keep the chunks' loads apart (register pressure)
+            if (Cf::kTmaStore && args.c_tma) {
+              store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
+            } else {
+              store_row_chunk(args, m, n_half + ch * 32, w);
+            }
           }
         }
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float(&w)[32] = *reinterpret_cast<float(*)[32]>(&v[ch * 32]);
-          if (Cf::kTmaStore && args.c_tma) {
-            store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
-          } else {
-            store_row_chunk(args, m, n_half + ch * 32, w);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) remote_arrive(tempty_leader0 + acc * 8);
+        if (u.role == kRoleContrib) {
+          __threadfence();
+          named_barrier_sync(1, kPairEpilogueThreads);
+          if (et == 0 && !(args.inject_drop && cta == args.drop_cta))
+            flag_release(args.flags + cta, args.epoch);
+        }
+      } else {
+        // Drain this thread's 128 columns, then hand the accumulator back.
+        float v[128];
+        __syncwarp();
+        tmem_load_64cols(t_row, reinterpret_cast<uint32_t*>(v));
+        tmem_load_64cols(t_row + 64, reinterpret_cast<uint32_t*>(v) + 64);
+        tmem_load_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) remote_arrive(tempty_leader0 + acc * 8);
+
+        if (u.role == kRoleContrib) {
+          float4* dst = reinterpret_cast<float4*>(args.P + cta * (kBM * kBN)) +
+                        static_cast<int64_t>(half * 4) * 8 * kBM + row;
+  #pragma unroll
+          for (int q = 0; q < 32; ++q)
+            __stcg(dst + q * kBM, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+          __threadfence();
+          named_barrier_sync(1, kPairEpilogueThreads);
+          if (et == 0 && !(args.inject_drop && cta == args.drop_cta))
+            flag_release(args.flags + cta, args.epoch);
+        } else if (status == kUnitStore) {
+          for (int c = 0; c < n_contrib; ++c) {
+            const float4* src =
+                reinterpret_cast<const float4*>(args.P + (2 * (pair + 1 + c) + rank) * (kBM * kBN)) +
+                static_cast<int64_t>(half * 4) * 8 * kBM + row;
+  #pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              float4 p[8];
+  #pragma unroll
+              for (int q = 0; q < 8; ++q) p[q] = __ldcg(src + (ch * 8 + q) * kBM);
+  #pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                v[ch * 32 + 4 * q] += p[q].x;
+                v[ch * 32 + 4 * q + 1] += p[q].y;
+                v[ch * 32 + 4 * q + 2] += p[q].z;
+                v[ch * 32 + 4 * q + 3] += p[q].w;
+              }
+              asm volatile("" ::: "memory");   // keep the chunks' loads apart (register pressure)
+            }
+          }
+  #pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            float(&w)[32] = *reinterpret_cast<float(*)[32]>(&v[ch * 32]);
+            if (Cf::kTmaStore && args.c_tma) {
+              store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
+            } else {
+              store_row_chunk(args, m, n_half + ch * 32, w);
+            }
           }
         }
       }
