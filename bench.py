@@ -434,7 +434,10 @@ def cpu_baseline(prob, seconds):
                                rows=(0, rows), threads=threads)
         return time.perf_counter() - t0
 
+    # two probes: a tiny one, then one of about a tenth of the budget, to estimate the rate
     probe_rows = min(prob.M, max(threads, 8))
+    t_probe = run(probe_rows)
+    probe_rows = int(min(prob.M, max(probe_rows, probe_rows * 0.1 * seconds / max(t_probe, 1e-3))))
     t_probe = run(probe_rows)
     rows = int(min(prob.M, max(probe_rows, probe_rows * seconds / max(t_probe, 1e-3))))
     rows = max(threads, rows - rows % threads) if rows >= threads else rows
