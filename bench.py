@@ -712,7 +712,8 @@ def extras(prob, sm_count, dist):
             cache[name] = Problem(name, prob.device)
         return cache[name]
 
-    for name in ["addmm_bf16_8192", "addmm_mxfp4_8192", "addmm_fp8_8192"]:
+    for name in ["addmm_bf16_8192", "addmm_mxfp4_8192", "addmm_fp8_8192",
+                 "gemm_bf16_1024x1024x16384"]:
         pr = get(name)
         peak = bpeak * {"bf16": 1.0, "mxfp4": FP4_OVER_BF16, "fp8": FP8_OVER_BF16}[pr.fmt]
         out[name] = _time_modes(pr, modes, sm_count, peak, dist)

@@ -150,6 +150,9 @@ WORKLOADS = {
                                        dict(operand_scale="sqrt_k", bias="none"), "bf16", 1238),
     "addmm_fp8_8192": ("fp8", 8192, 8192, 8192,
                        dict(operand_scale="sqrt_k", bias="bf16_uniform"), "bf16", 1239),
+    # few tiles, long K: 16 SM-pair tiles for 76 pairs, the case Stream-K exists for
+    "gemm_bf16_1024x1024x16384": ("bf16", 1024, 1024, 16384,
+                                  dict(operand_scale="sqrt_k", bias="none"), "bf16", 1241),
 }
 
 
