@@ -510,7 +510,8 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   const size_t P_bytes = streamk ? static_cast<size_t>(ctas) * kTileM * plan.tile_n * sizeof(float) : 0;
   const MxLayout mx = mx_layout(plan);
   Workspace* ws = nullptr;
-  if ((st = ensure_workspace(dev, stream, P_bytes, static_cast<size_t>(ctas),
+  // Flags are needed only where tiles are split (one per CTA); whole-tile grids use none.
+  if ((st = ensure_workspace(dev, stream, P_bytes, streamk ? static_cast<size_t>(ctas) : 0,
                              format == 1 ? mx.bytes() : 0, &ws)) != SK_OK)
     return st;
   if (++ws->epoch == 0) ws->epoch = 1;

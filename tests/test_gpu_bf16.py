@@ -299,3 +299,28 @@ def test_two_tile_hybrid_integer_inputs_are_bit_exact(shape, tile, num_sms, wave
                     options=dict(TILES[tile], hybrid_sk_waves=waves))
     want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), oracle.F32)
     assert np.array_equal(gu.host_bits(c), want.view(np.uint32))
+
+
+def test_whole_tile_grids_are_captured_beyond_the_reserved_grid():
+    # data-parallel and persistent launches split no tile: they need no Stream-K flags or
+    # slots, so a grid larger than the one reserved is still captured
+    M = N = 2048
+    K = 512
+    s = torch.cuda.Stream()
+    a = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    b = torch.empty((K, N), dtype=torch.bfloat16, device="cuda")
+    c = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    assert sk.sk_workspace_reserve(0, s.cuda_stream, 8) == sk.SK_OK
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        sk.gemm_bf16(a, b, None, out=c, out_dtype=torch.float32, mode="dp",
+                     options={"tile_m": 128, "tile_n": 128}, stream=s)   # 256 CTAs
+    p = inputs.bf16_problem(M, N, K, seed=4, integer=True)
+    a.copy_(gu.dev_bf16(p["A"]))
+    b.copy_(gu.dev_bf16(p["B"]))
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], None), oracle.F32)
+    assert np.array_equal(gu.host_bits(c), want.view(np.uint32))
