@@ -265,9 +265,11 @@ sk_status_t sk_gemm_bf16_static(const void* A, const void* B, const void* bias, 
 sk_status_t sk_stream_status(void* stream);
 
 /*
- * sk_workspace_reserve — size the workspace of (device, stream) for grids of up to max_grid
- * CTAs and MXFP4 problems of up to max_mx_m x max_mx_n x max_mx_k (0 = none), so that later
- * calls (e.g. while the stream is captured into a CUDA graph) need no allocation.
+ * sk_workspace_reserve — size the workspace of (device, stream) for Stream-K and hybrid grids
+ * of up to max_grid CTAs and MXFP4 problems of up to max_mx_m x max_mx_n x max_mx_k (0 = none),
+ * so that later calls (e.g. while the stream is captured into a CUDA graph) need no allocation.
+ * Data-parallel and persistent grids split no tile and use no per-CTA scratch, whatever their
+ * size; MXFP4 calls of every schedule use the scale scratch.
  */
 sk_status_t sk_workspace_reserve(int device, void* stream, int max_grid, int64_t max_mx_m,
                                  int64_t max_mx_n, int64_t max_mx_k);
