@@ -81,7 +81,7 @@ struct Cfg {
   static_assert(2 * kAccCols + (kMx ? kStages * (kSfaCols + kSfbCols) : 0) <= kTmemCols,
                 "tensor memory budget");
   static constexpr int kBarrierBytes = 256;
-  static_assert((2 * kStages + 5) * 8 + 20 <= kBarrierBytes, "barrier area");
+  static_assert((2 * kStages + 5) * 8 + 24 <= kBarrierBytes, "barrier area");
   // C leaves through TMA stores when its rows are 16-byte aligned: each epilogue warp stages
   // 32 rows x 64 bytes in one of its two 2 KB buffers.
   static constexpr int kEpiBytes = 4 * 2 * 2048;
@@ -167,6 +167,33 @@ __device__ __forceinline__ void add_partial8(float (&sum)[32], const float4 (&b)
   }
 }
 
+// Adds one contributor's partial (its P slot from `src`, fragment order, stride kBM float4s per
+// 4 columns) to this thread's row of `chunks` 32-column chunks held in tensor memory at
+// `t_stage`; the first contributor is copied.  The whole warp takes the same `first`.
+__device__ __forceinline__ void stage_partial(const float4* src, int chunks, uint32_t t_stage,
+                                              bool first) {
+#pragma unroll 1
+  for (int ch = 0; ch < chunks; ++ch) {
+    float4 pp[8];
+    load_partial8(pp, src + static_cast<int64_t>(ch) * 8 * kBM, kBM);
+    float sum[32];
+    if (first) {
+      add_partial8(sum, pp, true);
+    } else {
+      uint32_t prev[32];
+      __syncwarp();
+      tmem_load_32cols(t_stage + ch * 32, prev);
+      tmem_load_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sum[j] = __uint_as_float(prev[j]);
+      add_partial8(sum, pp, false);
+    }
+    __syncwarp();
+    tmem_store_32cols(t_stage + ch * 32, sum);
+  }
+  tmem_store_wait();
+}
+
 // Adds bias[n0 .. n0+32) (those below N) to v.
 __device__ __forceinline__ void add_bias_chunk(const Args& a, int64_t n0, float (&v)[32]) {
   if (a.bias == nullptr) return;
@@ -222,9 +249,12 @@ __device__ __forceinline__ bool tma_store_piece(const Args& a, const CUtensorMap
   if (x >= a.N || y >= a.M) return false;
   if (lane == 0) bulk_wait_read<1>();
   __syncwarp();
+  // C's tensor map uses the 64-byte swizzle: 16-byte chunk i of row r sits at chunk
+  // i ^ ((r >> 1) & 3), so the eight rows of each quarter-warp write eight different banks.
   uint4* dst = reinterpret_cast<uint4*>(buf + lane * 64);
+  const int sw = (lane >> 1) & 3;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) dst[i] = q[i];
+  for (int i = 0; i < 4; ++i) dst[i ^ sw] = q[i];
   fence_async_shared();
   __syncwarp();
   if (lane == 0) {
@@ -355,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* unit_status = tmem_slot + 2;   // two slots, indexed by accumulator
-  volatile uint32_t* staged_status = tmem_slot + 4; // partials staged in tensor memory
+  volatile uint32_t* staged_status = tmem_slot + 4; // two slots: partials staged in tensor memory
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -589,39 +619,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                                static_cast<uint32_t>(acc ^ 1) * Cf::kAccCols;
       uint32_t flag_status = kUnitStore;
       if (staged) {
-        if (et == 0) {
-          uint32_t st = kUnitStore;
-          for (int c = 0; c < n_contrib; ++c) {
+        // The farthest contributor first: it worked on this tile at the start of its range and
+        // is long done, while the nearest may still be on it.  Each partial is added as soon as
+        // its flag is seen.  (The status word alternates between two slots, so thread 0 never
+        // overwrites one that a slower thread has yet to read.)
+#pragma unroll 1
+        for (int i = 0; i < n_contrib; ++i) {
+          const int c = n_contrib - 1 - i;
+          if (et == 0) {
+            uint32_t st = kUnitStore;
             uint32_t* f = args.flags + cta + 1 + c;
             if (!wait_flag(f, args.epoch, args.timeout_ns)) {
               record_error(args, kSiteFlag, u.tile);
               st = kUnitSkip;
-              break;
+            } else {
+              *reinterpret_cast<volatile uint32_t*>(f) = 0u;  // consumed: ready for the next launch
             }
-            *reinterpret_cast<volatile uint32_t*>(f) = 0u;  // consumed: ready for the next launch
+            staged_status[i & 1] = st;
           }
-          *staged_status = st;
-        }
-        named_barrier_sync(1, kEpilogueThreads);
-        flag_status = *staged_status;
-        if (flag_status == kUnitStore) {
-#pragma unroll 1
-          for (int ch = 0; ch < kBN / 32; ++ch) {
-            const float4* src0 = reinterpret_cast<const float4*>(args.P + (cta + 1) * (kBM * kBN)) +
-                                 static_cast<int64_t>(ch) * 8 * kBM + row;
-            float sum[32];
-            float4 pp[8];
-            load_partial8(pp, src0, kBM);
-            add_partial8(sum, pp, true);
-#pragma unroll 1
-            for (int c = 1; c < n_contrib; ++c) {
-              load_partial8(pp, src0 + static_cast<int64_t>(c) * (kBM * kBN / 4), kBM);
-              add_partial8(sum, pp, false);
-            }
-            __syncwarp();
-            tmem_store_32cols(t_stage + ch * 32, sum);
-          }
-          tmem_store_wait();
+          named_barrier_sync(1, kEpilogueThreads);
+          flag_status = staged_status[i & 1];
+          if (flag_status != kUnitStore) break;
+          stage_partial(reinterpret_cast<const float4*>(args.P + (cta + 1 + c) * (kBM * kBN)) + row,
+                        kBN / 32, t_stage, i == 0);
         }
       }
       if (et == 0) {

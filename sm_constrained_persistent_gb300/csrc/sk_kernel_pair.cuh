@@ -166,7 +166,7 @@ struct PairCfg {
   static_assert(kAccBufs * kAccCols + (kMx ? kStages * (kSfaCols + kSfbCols) : 0) <= kTmemCols,
                 "tensor memory budget");
   static constexpr int kBarrierBytes = 512;
-  static_assert((3 * kStages + 6) * 8 + 20 <= kBarrierBytes, "barrier area");
+  static_assert((3 * kStages + 6) * 8 + 24 <= kBarrierBytes, "barrier area");
   static constexpr size_t kSmemBytes =
       1024 + static_cast<size_t>(kStages) * kStageBytes + kEpiBytes + kBarrierBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -207,7 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cp_done + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* unit_status = tmem_slot + 2;   // two slots, indexed by unit parity
-  volatile uint32_t* staged_status = tmem_slot + 4; // partials staged in tensor memory
+  volatile uint32_t* staged_status = tmem_slot + 4; // two slots: partials staged in tensor memory
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -478,42 +478,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
       const bool staged = Cf::kAccBufs == 2 && u.role == kRoleOwner && !has_next && n_contrib > 0;
       uint32_t flag_status = kUnitStore;
       if (staged) {
-        if (et == 0) {
-          uint32_t st = kUnitStore;
-          for (int c = 0; c < n_contrib; ++c) {
+        // The farthest contributor first (it is long done; the nearest may still be on this
+        // tile), each partial added as soon as its flag is seen; the status word alternates
+        // between two slots so thread 0 never overwrites one not yet read.
+        const uint32_t t_stage = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                 static_cast<uint32_t>(acc ^ 1) * Cf::kAccCols + half * 128;
+#pragma unroll 1
+        for (int i = 0; i < n_contrib; ++i) {
+          const int c = n_contrib - 1 - i;
+          if (et == 0) {
+            uint32_t st = kUnitStore;
             uint32_t* f = args.flags + 2 * (pair + 1 + c) + rank;
             if (!wait_flag(f, args.epoch, args.timeout_ns)) {
               record_error(args, kSiteFlag, u.tile);
               st = kUnitSkip;
-              break;
+            } else {
+              *reinterpret_cast<volatile uint32_t*>(f) = 0u;
             }
-            *reinterpret_cast<volatile uint32_t*>(f) = 0u;
+            staged_status[i & 1] = st;
           }
-          *staged_status = st;
-        }
-        named_barrier_sync(1, kPairEpilogueThreads);
-        flag_status = *staged_status;
-        if (flag_status == kUnitStore) {
-          const uint32_t t_stage = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   static_cast<uint32_t>(acc ^ 1) * Cf::kAccCols + half * 128;
-#pragma unroll 1
-          for (int ch = 0; ch < 4; ++ch) {
-            const float4* src0 =
-                reinterpret_cast<const float4*>(args.P + (2 * (pair + 1) + rank) * (kBM * kBN)) +
-                static_cast<int64_t>(half * 4 + ch) * 8 * kBM + row;
-            float sum[32];
-            float4 pp[8];
-            load_partial8(pp, src0, kBM);
-            add_partial8(sum, pp, true);
-#pragma unroll 1
-            for (int c = 1; c < n_contrib; ++c) {
-              load_partial8(pp, src0 + static_cast<int64_t>(2 * c) * (kBM * kBN / 4), kBM);
-              add_partial8(sum, pp, false);
-            }
-            __syncwarp();
-            tmem_store_32cols(t_stage + ch * 32, sum);
-          }
-          tmem_store_wait();
+          named_barrier_sync(1, kPairEpilogueThreads);
+          flag_status = staged_status[i & 1];
+          if (flag_status != kUnitStore) break;
+          stage_partial(reinterpret_cast<const float4*>(args.P + (2 * (pair + 1 + c) + rank) * (kBM * kBN)) +
+                            static_cast<int64_t>(half * 4) * 8 * kBM + row,
+                        4, t_stage, i == 0);
         }
       }
       if (et == 0) {
