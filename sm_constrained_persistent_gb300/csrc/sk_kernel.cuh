@@ -141,19 +141,46 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch,
                                           uint64_t timeout_ns) {
   if (flag_acquire(flag) == epoch) return true;
   const uint64_t t0 = global_timer_ns();
+  // Back off to at most ~128 ns between polls: one thread per CTA polls one word, and a
+  // longer sleep would be added to the fix-up of a tile whose contributor finishes last.
   uint32_t ns = 32;
   while (true) {
     __nanosleep(ns);
-    if (ns < 1024) ns <<= 1;
+    if (ns < 128) ns <<= 1;
     if (flag_acquire(flag) == epoch) return true;
     if (global_timer_ns() - t0 > timeout_ns) return false;
   }
 }
 
+// Thread 0 of an owner's epilogue while its piece's k-loop may still run: waits for the flag of
+// one contributor, unless the k-loop finishes first (the accumulator's full barrier `full`
+// completes phase `parity`) or the CTA is aborting.  kPollFlag: the flag was seen and consumed,
+// so the partial can be summed into the idle accumulator now.  kPollLoopDone: the partial is
+// left to the drain, which reads it while it stores C.  kPollTimeout: no flag within the limit.
+enum : uint32_t { kPollFlag = 0, kPollLoopDone = 1, kPollTimeout = 2 };
+__device__ __forceinline__ uint32_t poll_flag_or_full(uint32_t* flag, uint32_t epoch, uint64_t* full,
+                                                      uint32_t parity,
+                                                      volatile uint32_t* abort_flag,
+                                                      uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  uint32_t ns = 32;
+  while (true) {
+    if (mbar_test_wait(full, parity) || *abort_flag) return kPollLoopDone;
+    if (flag_acquire(flag) == epoch) {
+      *reinterpret_cast<volatile uint32_t*>(flag) = 0u;   // consumed: ready for the next launch
+      return kPollFlag;
+    }
+    if (global_timer_ns() - t0 > timeout_ns) return kPollTimeout;
+    __nanosleep(ns);
+    if (ns < 128) ns <<= 1;
+  }
+}
+
 // Eight float4 of one Stream-K partial (one 32-column chunk of a row), `stride` float4 apart.
 __device__ __forceinline__ void load_partial8(float4 (&b)[8], const float4* src, int stride) {
+  const uint64_t policy = l2_policy_evict_first();
 #pragma unroll
-  for (int q = 0; q < 8; ++q) b[q] = __ldcg(src + q * stride);
+  for (int q = 0; q < 8; ++q) b[q] = ld_cg_policy(src + q * stride, policy);
 }
 
 // sum = b (first) or sum += b, for one 32-column chunk.
@@ -168,28 +195,36 @@ __device__ __forceinline__ void add_partial8(float (&sum)[32], const float4 (&b)
 }
 
 // Adds one contributor's partial (its P slot from `src`, fragment order, stride kBM float4s per
-// 4 columns) to this thread's row of `chunks` 32-column chunks held in tensor memory at
-// `t_stage`; the first contributor is copied.  The whole warp takes the same `first`.
-__device__ __forceinline__ void stage_partial(const float4* src, int chunks, uint32_t t_stage,
-                                              bool first) {
+// 4 columns) to this thread's row of kChunks 32-column chunks held in tensor memory at
+// `t_stage`; the first contributor is copied.  The loads of kGroup chunks are issued together,
+// so a partial costs one round trip to L2 per kGroup chunks rather than one per chunk (kGroup
+// is what the kernel's register budget allows).  The whole warp takes the same `first`.
+template <int kChunks, int kGroup>
+__device__ __forceinline__ void stage_partial(const float4* src, uint32_t t_stage, bool first) {
+  static_assert(kChunks % kGroup == 0, "chunks are loaded kGroup at a time");
 #pragma unroll 1
-  for (int ch = 0; ch < chunks; ++ch) {
-    float4 pp[8];
-    load_partial8(pp, src + static_cast<int64_t>(ch) * 8 * kBM, kBM);
-    float sum[32];
-    if (first) {
-      add_partial8(sum, pp, true);
-    } else {
-      uint32_t prev[32];
-      __syncwarp();
-      tmem_load_32cols(t_stage + ch * 32, prev);
-      tmem_load_wait();
+  for (int g = 0; g < kChunks; g += kGroup) {
+    float4 pp[kGroup][8];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) sum[j] = __uint_as_float(prev[j]);
-      add_partial8(sum, pp, false);
+    for (int j = 0; j < kGroup; ++j)
+      load_partial8(pp[j], src + static_cast<int64_t>(g + j) * 8 * kBM, kBM);
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      float sum[32];
+      if (first) {
+        add_partial8(sum, pp[j], true);
+      } else {
+        uint32_t prev[32];
+        __syncwarp();
+        tmem_load_32cols(t_stage + (g + j) * 32, prev);
+        tmem_load_wait();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) sum[k] = __uint_as_float(prev[k]);
+        add_partial8(sum, pp[j], false);
+      }
+      __syncwarp();
+      tmem_store_32cols(t_stage + (g + j) * 32, sum);
     }
-    __syncwarp();
-    tmem_store_32cols(t_stage + ch * 32, sum);
   }
   tmem_store_wait();
 }
@@ -618,38 +653,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_stage = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                static_cast<uint32_t>(acc ^ 1) * Cf::kAccCols;
       uint32_t flag_status = kUnitStore;
+      int n_staged = 0;   // contributors summed into the idle accumulator (the farthest ones)
       if (staged) {
         // The farthest contributor first: it worked on this tile at the start of its range and
         // is long done, while the nearest may still be on it.  Each partial is added as soon as
-        // its flag is seen.  (The status word alternates between two slots, so thread 0 never
-        // overwrites one that a slower thread has yet to read.)
+        // its flag is seen, for as long as the k-loop runs; the rest are read by the drain.
+        // (The status word alternates between two slots, so thread 0 never overwrites one
+        // that a slower thread has yet to read.)
 #pragma unroll 1
         for (int i = 0; i < n_contrib; ++i) {
           const int c = n_contrib - 1 - i;
           if (et == 0) {
-            uint32_t st = kUnitStore;
-            uint32_t* f = args.flags + cta + 1 + c;
-            if (!wait_flag(f, args.epoch, args.timeout_ns)) {
-              record_error(args, kSiteFlag, u.tile);
-              st = kUnitSkip;
-            } else {
-              *reinterpret_cast<volatile uint32_t*>(f) = 0u;  // consumed: ready for the next launch
-            }
-            staged_status[i & 1] = st;
+            const uint32_t r = poll_flag_or_full(args.flags + cta + 1 + c, args.epoch, &tfull[acc],
+                                                 acc_phase, abort_flag, args.timeout_ns);
+            if (r == kPollTimeout) record_error(args, kSiteFlag, u.tile);
+            staged_status[i & 1] = r;
           }
           named_barrier_sync(1, kEpilogueThreads);
-          flag_status = staged_status[i & 1];
-          if (flag_status != kUnitStore) break;
-          stage_partial(reinterpret_cast<const float4*>(args.P + (cta + 1 + c) * (kBM * kBN)) + row,
-                        kBN / 32, t_stage, i == 0);
+          const uint32_t r = staged_status[i & 1];
+          if (r == kPollLoopDone) break;
+          if (r == kPollTimeout) {
+            flag_status = kUnitSkip;
+            break;
+          }
+          stage_partial<kBN / 32, 2>(
+              reinterpret_cast<const float4*>(args.P + (cta + 1 + c) * (kBM * kBN)) + row, t_stage,
+              i == 0);
+          n_staged = i + 1;
         }
       }
+      // contributors 0 .. n_rem-1 (the nearest) are read by the drain
+      const int n_rem = flag_status == kUnitStore ? n_contrib - n_staged : 0;
       if (et == 0) {
         uint32_t status = kUnitStore;
         if (!wait_bar(&tfull[acc], acc_phase, abort_flag, args, kSiteEpilogue)) {
           status = kUnitAbort;
-        } else if (u.role == kRoleOwner && !staged) {
-          for (int c = 0; c < n_contrib; ++c) {
+        } else if (u.role == kRoleOwner) {
+          for (int c = 0; c < n_rem; ++c) {
             uint32_t* f = args.flags + cta + 1 + c;
             if (!wait_flag(f, args.epoch, args.timeout_ns)) {
               record_error(args, kSiteFlag, u.tile);
@@ -670,13 +710,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc) * Cf::kAccCols;
       float4* my_slot = reinterpret_cast<float4*>(args.P + cta * (kBM * kBN));
+      // Partials not summed during the k-loop are read here: two contributors' chunks in
+      // flight at a time, the next chunk's requested before this one is stored, so the round
+      // trips to L2 overlap the drain's other work.
+      constexpr int64_t kSlot4 = kBM * kBN / 4;   // float4s between consecutive CTAs' slots
+      const float4* rem0 = reinterpret_cast<const float4*>(args.P + (cta + 1) * (kBM * kBN)) + row;
+      float4 pp[8], pq[8];
+      if (do_store && n_rem > 0) load_partial8(pp, rem0, kBM);
+      if (do_store && n_rem > 1) load_partial8(pq, rem0 + kSlot4, kBM);
 #pragma unroll 1
       for (int ch = 0; ch < kBN / 32; ++ch) {
+        const float4* rem = rem0 + static_cast<int64_t>(ch) * 8 * kBM;
         uint32_t r[32];
         __syncwarp();
         tmem_load_32cols(t_row + ch * 32, r);
         float v[32];
-        if (staged) {
+        if (n_staged > 0) {
           uint32_t part[32];
           tmem_load_32cols(t_stage + ch * 32, part);
           tmem_load_wait();
@@ -690,23 +739,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u.role == kRoleContrib) {
           // Slot layout [chunk][column quad][row]: one warp store covers 512 contiguous bytes.
           float4* dst = my_slot + static_cast<int64_t>(ch) * 8 * kBM + row;
+          const uint64_t policy = l2_policy_evict_last();
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            __stcg(dst + q * kBM, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+            st_cg_policy(dst + q * kBM, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]),
+                         policy);
         } else if (do_store) {
-          if (!staged) {
-            for (int c = 0; c < n_contrib; ++c) {
-              const float4* src =
-                  reinterpret_cast<const float4*>(args.P + (cta + 1 + c) * (kBM * kBN)) +
-                  static_cast<int64_t>(ch) * 8 * kBM + row;
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                const float4 p = __ldcg(src + q * kBM);
-                v[4 * q] += p.x;
-                v[4 * q + 1] += p.y;
-                v[4 * q + 2] += p.z;
-                v[4 * q + 3] += p.w;
-              }
+          if (n_rem > 0) {
+            add_partial8(v, pp, false);
+            if (n_rem > 1) add_partial8(v, pq, false);
+#pragma unroll 1
+            for (int c = 2; c < n_rem; c += 2) {
+              load_partial8(pp, rem + c * kSlot4, kBM);
+              if (c + 1 < n_rem) load_partial8(pq, rem + (c + 1) * kSlot4, kBM);
+              add_partial8(v, pp, false);
+              if (c + 1 < n_rem) add_partial8(v, pq, false);
+            }
+            if (ch + 1 < kBN / 32) {
+              load_partial8(pp, rem + 8 * kBM, kBM);
+              if (n_rem > 1) load_partial8(pq, rem + 8 * kBM + kSlot4, kBM);
             }
           }
           if (args.c_tma) {

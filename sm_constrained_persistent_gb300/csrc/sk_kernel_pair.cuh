@@ -477,40 +477,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
       // idle accumulator held the previous piece, already drained; no later piece uses it.)
       const bool staged = Cf::kAccBufs == 2 && u.role == kRoleOwner && !has_next && n_contrib > 0;
       uint32_t flag_status = kUnitStore;
+      int n_staged = 0;   // contributors summed into the idle accumulator (the farthest ones)
       if (staged) {
         // The farthest contributor first (it is long done; the nearest may still be on this
-        // tile), each partial added as soon as its flag is seen; the status word alternates
-        // between two slots so thread 0 never overwrites one not yet read.
+        // tile), each partial added as soon as its flag is seen, for as long as the k-loop
+        // runs; the rest are read by the drain.  The status word alternates between two slots
+        // so thread 0 never overwrites one not yet read.
         const uint32_t t_stage = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                  static_cast<uint32_t>(acc ^ 1) * Cf::kAccCols + half * 128;
 #pragma unroll 1
         for (int i = 0; i < n_contrib; ++i) {
           const int c = n_contrib - 1 - i;
           if (et == 0) {
-            uint32_t st = kUnitStore;
-            uint32_t* f = args.flags + 2 * (pair + 1 + c) + rank;
-            if (!wait_flag(f, args.epoch, args.timeout_ns)) {
-              record_error(args, kSiteFlag, u.tile);
-              st = kUnitSkip;
-            } else {
-              *reinterpret_cast<volatile uint32_t*>(f) = 0u;
-            }
-            staged_status[i & 1] = st;
+            const uint32_t r =
+                poll_flag_or_full(args.flags + 2 * (pair + 1 + c) + rank, args.epoch, &tfull[acc],
+                                  acc_phase, abort_flag, args.timeout_ns);
+            if (r == kPollTimeout) record_error(args, kSiteFlag, u.tile);
+            staged_status[i & 1] = r;
           }
           named_barrier_sync(1, kPairEpilogueThreads);
-          flag_status = staged_status[i & 1];
-          if (flag_status != kUnitStore) break;
-          stage_partial(reinterpret_cast<const float4*>(args.P + (2 * (pair + 1 + c) + rank) * (kBM * kBN)) +
-                            static_cast<int64_t>(half * 4) * 8 * kBM + row,
-                        4, t_stage, i == 0);
+          const uint32_t r = staged_status[i & 1];
+          if (r == kPollLoopDone) break;
+          if (r == kPollTimeout) {
+            flag_status = kUnitSkip;
+            break;
+          }
+          stage_partial<4, 2>(reinterpret_cast<const float4*>(args.P + (2 * (pair + 1 + c) + rank) * (kBM * kBN)) +
+                               static_cast<int64_t>(half * 4) * 8 * kBM + row,
+                           t_stage, i == 0);
+          n_staged = i + 1;
         }
       }
+      // contributors 0 .. n_rem-1 (the nearest) are read by the drain
+      const int n_rem = flag_status == kUnitStore ? n_contrib - n_staged : 0;
       if (et == 0) {
         uint32_t status = kUnitStore;
         if (!wait_bar(&tfull[acc], acc_phase, abort_flag, args, kSiteEpilogue)) {
           status = kUnitAbort;
-        } else if (u.role == kRoleOwner && !staged) {
-          for (int c = 0; c < n_contrib; ++c) {
+        } else if (u.role == kRoleOwner) {
+          for (int c = 0; c < n_rem; ++c) {
             uint32_t* f = args.flags + 2 * (pair + 1 + c) + rank;
             if (!wait_flag(f, args.epoch, args.timeout_ns)) {
               record_error(args, kSiteFlag, u.tile);
@@ -531,20 +536,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
 
       if (staged) {
         // Last piece: no later piece waits for this accumulator, so add and store it 32
-        // columns at a time, then release it as usual.
+        // columns at a time, then release it as usual.  The partials not summed during the
+        // k-loop are read here.
         const bool store = status == kUnitStore && flag_status == kUnitStore;
         const uint32_t t_stage = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                  static_cast<uint32_t>(acc ^ 1) * Cf::kAccCols + half * 128;
+        const float4* rem0 =
+            reinterpret_cast<const float4*>(args.P + (2 * (pair + 1) + rank) * (kBM * kBN)) +
+            static_cast<int64_t>(half * 4) * 8 * kBM + row;
+        constexpr int64_t kSlot4 = 2 * (kBM * kBN / 4);   // float4s between consecutive pairs' slots
+        // Two contributors' chunks are in flight at a time, and the next chunk's are requested
+        // before this chunk is stored, so the round trips to L2 overlap the drain's other work.
+        float4 pp[8], pq[8];
+        if (store && n_rem > 0) load_partial8(pp, rem0, kBM);
+        if (store && n_rem > 1) load_partial8(pq, rem0 + kSlot4, kBM);
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
-          uint32_t own[32], part[32];
+          const float4* rem = rem0 + static_cast<int64_t>(ch) * 8 * kBM;
+          uint32_t own[32];
           __syncwarp();
           tmem_load_32cols(t_row + ch * 32, own);
-          tmem_load_32cols(t_stage + ch * 32, part);
-          tmem_load_wait();
           float w[32];
+          if (n_staged > 0) {
+            uint32_t part[32];
+            tmem_load_32cols(t_stage + ch * 32, part);
+            tmem_load_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(own[j]) + __uint_as_float(part[j]);
+            for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(own[j]) + __uint_as_float(part[j]);
+          } else {
+            tmem_load_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(own[j]);
+          }
+          if (store && n_rem > 0) {
+            add_partial8(w, pp, false);
+            if (n_rem > 1) add_partial8(w, pq, false);
+#pragma unroll 1
+            for (int c = 2; c < n_rem; c += 2) {
+              load_partial8(pp, rem + c * kSlot4, kBM);
+              if (c + 1 < n_rem) load_partial8(pq, rem + (c + 1) * kSlot4, kBM);
+              add_partial8(w, pp, false);
+              if (c + 1 < n_rem) add_partial8(w, pq, false);
+            }
+            if (ch + 1 < 4) {
+              load_partial8(pp, rem + 8 * kBM, kBM);
+              if (n_rem > 1) load_partial8(pq, rem + 8 * kBM + kSlot4, kBM);
+            }
+          }
           if (store) {
             if (Cf::kTmaStore && args.c_tma) {
               store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
@@ -575,9 +613,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
           for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(r[j]);
           if (u.role == kRoleContrib) {
             float4* dst = my_slot + static_cast<int64_t>(ch) * 8 * kBM;
+            const uint64_t policy = l2_policy_evict_last();
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              __stcg(dst + q * kBM, make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
+              st_cg_policy(dst + q * kBM, make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]),
+                           policy);
           } else if (status == kUnitStore) {
             for (int c = 0; c < n_contrib; ++c) {
               const float4* src =
@@ -617,14 +657,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
         if (u.role == kRoleContrib) {
           float4* dst = reinterpret_cast<float4*>(args.P + cta * (kBM * kBN)) +
                         static_cast<int64_t>(half * 4) * 8 * kBM + row;
+          const uint64_t policy = l2_policy_evict_last();
   #pragma unroll
           for (int q = 0; q < 32; ++q)
-            __stcg(dst + q * kBM, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+            st_cg_policy(dst + q * kBM, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]),
+                         policy);
           __threadfence();
           named_barrier_sync(1, kPairEpilogueThreads);
           if (et == 0 && !(args.inject_drop && cta == args.drop_cta))
             flag_release(args.flags + cta, args.epoch);
         } else if (status == kUnitStore) {
+          const uint64_t policy = l2_policy_evict_first();
           for (int c = 0; c < n_contrib; ++c) {
             const float4* src =
                 reinterpret_cast<const float4*>(args.P + (2 * (pair + 1 + c) + rank) * (kBM * kBN)) +
@@ -633,7 +676,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
             for (int ch = 0; ch < 4; ++ch) {
               float4 p[8];
   #pragma unroll
-              for (int q = 0; q < 8; ++q) p[q] = __ldcg(src + (ch * 8 + q) * kBM);
+              for (int q = 0; q < 8; ++q) p[q] = ld_cg_policy(src + (ch * 8 + q) * kBM, policy);
   #pragma unroll
               for (int q = 0; q < 8; ++q) {
                 v[ch * 32 + 4 * q] += p[q].x;

@@ -52,6 +52,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking test of a phase (try_wait may suspend the thread for a while first).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // ---- TMA (bulk tensor / bulk copies into shared memory) ----------------------------------
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
@@ -251,6 +264,36 @@ constexpr uint32_t kLayoutSwizzleNone = 0;
 constexpr uint32_t kLayoutSwizzle128B = 2;
 
 // ---- cross-CTA flags (Stream-K fixup) ------------------------------------------------------
+
+// L2 cache policies (PTX createpolicy): Stream-K partials are written with evict_last, so they
+// outlast the operand tiles streaming through L2 until their owner reads them, and read with
+// evict_first, since nothing reads them again.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// st.global.cg / ld.global.cg of a float4 with an L2 cache policy.
+__device__ __forceinline__ void st_cg_policy(float4* ptr, float4 v, uint64_t policy) {
+  asm volatile("st.global.cg.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ float4 ld_cg_policy(const float4* ptr, uint64_t policy) {
+  float4 v;
+  asm volatile("ld.global.cg.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(ptr), "l"(policy));
+  return v;
+}
 
 __device__ __forceinline__ void flag_release(uint32_t* flag, uint32_t value) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(value) : "memory");
