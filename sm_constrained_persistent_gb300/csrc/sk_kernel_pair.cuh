@@ -475,7 +475,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
       // partials of the CTAs that continue it are summed into the idle accumulator, so the
       // fix-up after the loop reads tensor memory instead of waiting on global memory.  (The
       // idle accumulator held the previous piece, already drained; no later piece uses it.)
-      const bool staged = Cf::kAccBufs == 2 && u.role == kRoleOwner && !has_next && n_contrib > 0;
+      // The shared tile an owner finishes with: no later piece waits for its accumulator, so it
+      // is drained from tensor memory 32 columns at a time with the partials added (below).
+      const bool last_shared = u.role == kRoleOwner && !has_next && n_contrib > 0;
+      const bool staged = Cf::kAccBufs == 2 && last_shared;
       uint32_t flag_status = kUnitStore;
       int n_staged = 0;   // contributors summed into the idle accumulator (the farthest ones)
       if (staged) {
@@ -534,7 +537,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc) * Cf::kAccCols + half * 128;
 
-      if (staged) {
+      if (last_shared) {
         // Last piece: no later piece waits for this accumulator, so add and store it 32
         // columns at a time, then release it as usual.  The partials not summed during the
         // k-loop are read here.
