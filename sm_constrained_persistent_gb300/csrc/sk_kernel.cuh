@@ -1,7 +1,7 @@
 // The addmm GEMM kernel for sm_103a: C = A * B (+ bias[n]), fp32 accumulation in tensor
-// memory, for bf16 operands (tcgen05 kind::f16) and MXFP4 operands (tcgen05 kind::mxf4 with
-// E8M0 block scales), under the data-parallel, SM-constrained persistent, Stream-K and hybrid
-// schedules of sk_schedule.cuh.
+// memory, for bf16 operands (tcgen05 kind::f16), fp8 E4M3 operands (kind::f8f6f4) and MXFP4
+// operands (kind::mxf4 with E8M0 block scales), under the data-parallel, SM-constrained
+// persistent, Stream-K and hybrid schedules of sk_schedule.cuh.
 //
 // One CTA of 192 threads per SM, warp-specialised:
 //   warp 0      TMA producer: streams the A and B tiles of every k-iteration (and the MXFP4
@@ -12,7 +12,8 @@
 //               epilogue of one tile overlaps the main loop of the next.
 //   warps 2..5  epilogue, thread = tile row: tensor memory -> registers, then by role
 //                 whole tile / owner:  (+ partials of the contributors) + bias[n] -> cast ->
-//                                      store C;
+//                                      store C (TMA stores from shared memory where C's
+//                                      rows are 16-byte aligned);
 //                 contribution:        fp32 partial -> this CTA's scratch slot P[cta] with
 //                                      coalesced 16-byte stores, then a release of
 //                                      flags[cta].
@@ -646,9 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // A shared tile that is this CTA's last piece: while its k-loop still runs, the
-      // contributors' partials are summed into the idle accumulator (which held the previous
-      // piece, already drained; no later piece uses it), so the fix-up after the loop reads
-      // tensor memory instead of waiting on global memory.
+      // contributors' partials that are already complete are summed into the idle accumulator
+      // (which held the previous piece, already drained; no later piece uses it); the drain
+      // after the loop reads the rest.
       const bool staged = u.role == kRoleOwner && !has_next && n_contrib > 0;
       const uint32_t t_stage = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                static_cast<uint32_t>(acc ^ 1) * Cf::kAccCols;

@@ -12,9 +12,10 @@
 //               cta_group::2 MMAs and commits them to the "empty" and "accumulator full"
 //               barriers of both CTAs at once (multicast).
 //   warps 2..9  epilogue, two warps per 32-lane quarter: warp w reads lanes 32*(w%4).. and
-//               columns [128*h, 128*h+128), h = (w-2)/4.  Each thread first drains its 128
-//               accumulator columns into registers and releases the accumulator to the
-//               leader, then spills (contribution) or aggregates + bias + casts + stores.
+//               columns [128*h, 128*h+128), h = (w-2)/4.  Each thread drains its row 32
+//               columns at a time (bf16, fp8) or all 128 into registers at once (MXFP4), spills
+//               them (contribution) or adds partials + bias, casts and stores them, and then
+//               releases the accumulator to the leader.
 //   warp 10     (MXFP4 only) in the leader, one lane copies each stage's scale factors from
 //               shared to tensor memory (tcgen05.cp) and commits them to that stage's
 //               "scales ready" barrier, which the MMA thread waits on; keeping the copies off
@@ -471,12 +472,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
           covered += (len < plan.iters - covered) ? len : (plan.iters - covered);
         }
       }
-      // A shared tile that is this CTA's last piece: while its k-loop still runs, the
-      // partials of the CTAs that continue it are summed into the idle accumulator, so the
-      // fix-up after the loop reads tensor memory instead of waiting on global memory.  (The
-      // idle accumulator held the previous piece, already drained; no later piece uses it.)
       // The shared tile an owner finishes with: no later piece waits for its accumulator, so it
       // is drained from tensor memory 32 columns at a time with the partials added (below).
+      // With two accumulators, partials that are complete while its k-loop still runs are
+      // summed into the idle one meanwhile (it held the previous piece, already drained; no
+      // later piece uses it), so the fix-up after the loop reads tensor memory.
       const bool last_shared = u.role == kRoleOwner && !has_next && n_contrib > 0;
       const bool staged = Cf::kAccBufs == 2 && last_shared;
       uint32_t flag_status = kUnitStore;
