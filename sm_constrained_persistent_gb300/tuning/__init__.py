@@ -105,7 +105,10 @@ def fit(times, sm_count=152):
     for shape in times:
         rs = [(r, p) for r, p in zip(rows, pred) if r[0] == shape]
         best = min(r[3] for r, _ in rs)
-        pick = min(((r, p) for r, p in rs if r[2] != "dp"), key=lambda t: t[1])[0]
+        M = int(shape.split("x")[0])
+        # the planner's candidates: no data-parallel, and no 128x256 tile for one row of tiles
+        pick = min(((r, p) for r, p in rs if r[2] != "dp" and not (M <= 128 and r[1] == "128x256")),
+                   key=lambda t: t[1])[0]
         losses.append(pick[3] / best - 1.0)
     names = ["t_iter_pair", "t_iter_128x256", "t_iter_128x128", "t_piece", "t_split", "t_part",
              "t_launch", "t_dp_wave"]

@@ -172,6 +172,12 @@ def test_auto_mode_picks_a_concrete_plan_from_the_cost_model():
         assert p.mode in (1, 2, 3)
         rows = sk.sk_plan_segments(p)          # a concrete plan: its segments cover every tile
         assert rows[:, 3].sum() - rows[:, 2].sum() == p.tiles * p.iters
+    # one row of tiles streams B through 128-column tiles, unless a tile is forced
+    for (M, N, K) in [(96, 8192, 8192), (64, 14336, 4096), (128, 4096, 11008), (1, 4096, 4096)]:
+        p = sk.sk_plan(0, M, N, K, 0, "auto", 152)
+        assert (p.tile_m, p.tile_n) == (128, 128), (M, N, K)
+    p = sk.sk_plan(0, 96, 8192, 8192, 0, "auto", 152, {"tile_n": 256})
+    assert (p.tile_m, p.tile_n) == (128, 256)
     # tiles the options force stay forced; MXFP4 never gets a 128x256 tile
     p = sk.sk_plan(0, 8192, 8192, 8192, 0, "auto", 152, {"tile_m": 128, "tile_n": 128})
     assert (p.tile_m, p.tile_n) == (128, 128)
