@@ -27,6 +27,8 @@
  *                       cost model fitted to GB300 timings: launch + per-k-iteration time of
  *                       the tile kind x the iterations of the busiest CTA + a cost per piece of
  *                       work + a Stream-K fix-up cost per split tile and per CTA sharing it.
+ *                       A problem with one row of tiles (M <= 128), bound by streaming B,
+ *                       does not get 128 x 256 tiles unless the options force them.
  *                       This is the tuning step the SM-constraint GEMM page lists as optional
  *                       (flashinfer PR #982, "tune: get best config for gemm").  sk_plan()
  *                       reports the choice (its `mode` field holds the schedule picked).
