@@ -287,7 +287,7 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D tensor map over a row-major matrix [rows][cols] of `elem` bytes per element, boxes of
-// box_cols x box_rows elements, 128-byte swizzle, zero fill outside the matrix.
+// box_cols x box_rows elements, `swizzle` (128-byte unless given), zero fill outside the matrix.
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, size_t elem, const void* base,
                int64_t rows, int64_t cols, uint32_t box_cols, uint32_t box_rows,
                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
