@@ -324,3 +324,30 @@ def test_whole_tile_grids_are_captured_beyond_the_reserved_grid():
     torch.cuda.synchronize()
     want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], None), oracle.F32)
     assert np.array_equal(gu.host_bits(c), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("mode", ["streamk", "hybrid"])
+@pytest.mark.parametrize("shape,tile,num_sms", [
+    ((512, 512, 8192), "pair256", 0),      # 4 pair tiles on 76 pairs: ~19 pieces per tile
+    ((1920, 1920, 2048), "pair256", 0),    # 64 tiles on 76 pairs: pairs working inside one tile
+    ((1920, 1920, 2048), "pair256", 90),   # 45 pairs
+    ((640, 640, 4096), "128x256", 0),      # 15 tiles on 152 CTAs: ~10 pieces per tile
+    ((512, 512, 8192), "128x128", 0),      # 16 tiles on 152 CTAs
+    ((1920, 1920, 2048), "128x128", 7),    # long ranges over many tiles on 7 CTAs
+])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_streamk_fixup_with_many_and_late_contributors_is_bit_exact(mode, shape, tile, num_sms, out):
+    # Every partial must be added exactly once, whether the owner summed it into its idle
+    # accumulator during its k-loop or read it in its drain: exact on integer inputs.
+    M, N, K = shape
+    p = inputs.bf16_problem(M, N, K, seed=M + N + K + num_sms, integer=True,
+                            bias="bf16_int" if out == "bf16" else "f32_int")
+    plan = sk.sk_plan(0, M, N, K, num_sms, mode, torch.cuda.get_device_properties(0).multi_processor_count,
+                      TILES[tile])
+    assert plan.sk_tiles > 0
+    want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]),
+                               oracle.BF16 if out == "bf16" else oracle.F32)
+    want_bits = want if out == "bf16" else want.view(np.uint32)
+    for _ in range(2):   # the second launch reuses flags the first one's owners cleared
+        c = gu.run_bf16(p, out=out, mode=mode, num_sms=num_sms, options=TILES[tile])
+        assert np.array_equal(gu.host_bits(c), want_bits)
