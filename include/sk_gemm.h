@@ -283,10 +283,11 @@ void sk_workspace_release_all(void);
 const char* sk_status_string(sk_status_t status);
 
 /*
- * sk_device_caps — what the library can launch on `device` (prepares every kernel variant on
- * it): SM count, compute capability, resident CTAs per SM of the one-CTA-per-tile variants
- * (bf16 128x128, bf16 128x256, MXFP4 128x128) and resident 2-CTA clusters of the SM-pair
- * variants (bf16 and MXFP4 256x256), with the CUDA error (0 = none) of each variant's set-up.
+ * sk_device_caps — what the library can launch on `device` (prepares every kernel variant of
+ * the plain operand layouts on it): SM count, compute capability, resident CTAs per SM of the
+ * one-CTA-per-tile variants (bf16 128x128, bf16 128x256, MXFP4 128x128; fp8 128x128 and
+ * 128x256) and resident 2-CTA clusters of the SM-pair variants (bf16, MXFP4 and fp8 256x256),
+ * with the CUDA error (0 = none) of each variant's set-up.
  */
 typedef struct {
   int32_t sm_count;
@@ -294,6 +295,9 @@ typedef struct {
   int32_t ctas_per_sm[3];        /* bf16 128x128, bf16 128x256, MXFP4 128x128   */
   int32_t max_pair_clusters[2];  /* bf16 256x256 pairs, MXFP4 256x256 pairs      */
   int32_t setup_error[5];        /* cudaError_t of each variant's set-up, in the order above */
+  int32_t fp8_ctas_per_sm[2];    /* fp8 128x128, fp8 128x256                     */
+  int32_t fp8_max_pair_clusters; /* fp8 256x256 pairs                            */
+  int32_t fp8_setup_error[3];    /* fp8 128x128, 128x256, 256x256 pairs          */
 } sk_device_caps_t;
 
 sk_status_t sk_device_caps(int device, sk_device_caps_t* caps);

@@ -54,7 +54,9 @@ class DeviceCaps(ctypes.Structure):
     """sk_device_caps_t."""
     _fields_ = [("sm_count", ctypes.c_int32), ("cc_major", ctypes.c_int32),
                 ("cc_minor", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32 * 3),
-                ("max_pair_clusters", ctypes.c_int32 * 2), ("setup_error", ctypes.c_int32 * 5)]
+                ("max_pair_clusters", ctypes.c_int32 * 2), ("setup_error", ctypes.c_int32 * 5),
+                ("fp8_ctas_per_sm", ctypes.c_int32 * 2), ("fp8_max_pair_clusters", ctypes.c_int32),
+                ("fp8_setup_error", ctypes.c_int32 * 3)]
 
 
 def library_path() -> str:
@@ -223,7 +225,9 @@ def sk_device_caps(device=0):
         raise SkError(st, "sk_device_caps")
     return {"sm_count": c.sm_count, "cc": (c.cc_major, c.cc_minor),
             "ctas_per_sm": list(c.ctas_per_sm), "max_pair_clusters": list(c.max_pair_clusters),
-            "setup_error": list(c.setup_error)}
+            "setup_error": list(c.setup_error), "fp8_ctas_per_sm": list(c.fp8_ctas_per_sm),
+            "fp8_max_pair_clusters": c.fp8_max_pair_clusters,
+            "fp8_setup_error": list(c.fp8_setup_error)}
 
 
 def sk_plan(fmt, M, N, K, num_sms, mode, sm_count, options=None):

@@ -816,6 +816,13 @@ sk_status_t sk_device_caps(int device, sk_device_caps_t* caps) {
         caps->max_pair_clusters[0] = d->max_pairs[sk::kVariantBf16Pair];
         caps->max_pair_clusters[1] = d->max_pairs[sk::kVariantMxPair];
         for (int i = 0; i < 5; ++i) caps->setup_error[i] = d->setup_error[reported[i]];
+        const int fp8[3] = {sk::variant_of(sk::kKindF8N128, 0), sk::variant_of(sk::kKindF8N256, 0),
+                            sk::variant_of(sk::kKindF8Pair, 0)};
+        for (int i = 0; i < 3; ++i) ensure_variant(*d, fp8[i]);
+        caps->fp8_ctas_per_sm[0] = d->ctas_per_sm[fp8[0]];
+        caps->fp8_ctas_per_sm[1] = d->ctas_per_sm[fp8[1]];
+        caps->fp8_max_pair_clusters = d->max_pairs[fp8[2]];
+        for (int i = 0; i < 3; ++i) caps->fp8_setup_error[i] = d->setup_error[fp8[i]];
       } else {
         st = SK_ERR_UNSUPPORTED;
       }

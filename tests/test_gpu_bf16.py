@@ -214,6 +214,9 @@ def test_device_caps_report_the_pair_capacity():
     assert caps["setup_error"] == [0] * 5
     assert all(n >= 1 for n in caps["ctas_per_sm"])
     assert all(2 * n <= caps["sm_count"] and n >= 1 for n in caps["max_pair_clusters"])
+    assert caps["fp8_setup_error"] == [0] * 3
+    assert all(n >= 1 for n in caps["fp8_ctas_per_sm"])
+    assert 1 <= caps["fp8_max_pair_clusters"] and 2 * caps["fp8_max_pair_clusters"] <= caps["sm_count"]
 
 
 def test_streamk_wait_that_runs_out_reports_timeout():
