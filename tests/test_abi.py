@@ -178,6 +178,8 @@ def test_auto_mode_picks_a_concrete_plan_from_the_cost_model():
         assert (p.tile_m, p.tile_n) == (128, 128), (M, N, K)
     p = sk.sk_plan(0, 96, 8192, 8192, 0, "auto", 152, {"tile_n": 256})
     assert (p.tile_m, p.tile_n) == (128, 256)
+    p = sk.sk_plan(2, 96, 8192, 8192, 0, "auto", 152)        # fp8 follows the same rule
+    assert (p.tile_m, p.tile_n) == (128, 128)
     # tiles the options force stay forced; MXFP4 never gets a 128x256 tile
     p = sk.sk_plan(0, 8192, 8192, 8192, 0, "auto", 152, {"tile_m": 128, "tile_n": 128})
     assert (p.tile_m, p.tile_n) == (128, 128)
