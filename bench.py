@@ -36,6 +36,9 @@ FP4_OVER_BF16 = 13.5 / 2.25
 # fp8 dense peak relative to bf16 dense (nominal 4.5 / 2.25 PFLOP/s)
 FP8_OVER_BF16 = 4.5 / 2.25
 FORMAT_CODE = {"bf16": 0, "mxfp4": 1, "fp8": 2}
+# Nominal dense tensor peaks of one GB300 the targets are stated against (TFLOP/s): bf16
+# ~2.25 PFLOP/s, fp8 4.5, FP4 ~9 PFLOP/s.
+NOMINAL_DENSE_TFLOPS = {"bf16": 2250.0, "fp8": 4500.0, "mxfp4": 9000.0}
 DTYPE_NAME = {"bf16": "bf16", "mxfp4": "mxfp4(e2m1+e8m0)", "fp8": "fp8(e4m3)"}
 
 
@@ -524,7 +527,8 @@ def run_ours(args):
                    "num_sms": args.num_sms if args.num_sms > 0 else sm_count,
                    "grid": plan.grid, "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}",
                    "tile_quant_eff": round(tile_efficiency(plan, sm_count, args.num_sms), 4),
-                   "pct_of_dense_peak": round(100 * value / world / peak, 2),
+                   "pct_of_measured_peak": round(100 * value / world / peak, 2),
+                   "pct_of_nominal_peak": round(100 * value / world / NOMINAL_DENSE_TFLOPS[prob.fmt], 2),
                    "l2": ("L2 flushed before each step (256 MiB write, then a 256 MiB read so "
                           "the lines left are clean)" if needs_flush(prob)
                           else "inputs larger than L2 (no flush)"),
@@ -538,10 +542,88 @@ def run_ours(args):
         result["extras"] = extras(prob, sm_count, dist)
     if world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(prob, args.cpu_seconds)
+    # last key: the per-config, per-schedule figures in a form short enough to survive a
+    # truncated log tail
+    result["summary"] = summary_block(result, args.mode, prob.fmt, peak)
     if rank == 0:
-        print(json.dumps(result), flush=True)
+        print(json.dumps(result, separators=(",", ":")), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+MODE_KEY = {"dp": "dp", "persistent": "pe", "streamk": "sk", "hybrid": "hy", "auto": "au"}
+
+
+def summary_block(result, mode, fmt, measured_peak):
+    """Compact per-config x schedule table: [ms, TFLOPS, % of nominal dense peak, % of measured
+    peak, tile-quantisation efficiency] per schedule (dp, pe = persistent, sk = Stream-K,
+    hy = hybrid); the num_sms sweeps as [ms, TFLOPS or GB/s, SMs used]."""
+    peaks, _ = measured_peaks()
+    bpeak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    meas = {"bf16": bpeak, "fp8": bpeak * FP8_OVER_BF16, "mxfp4": bpeak * FP4_OVER_BF16}
+
+    def row(r, f):
+        t = r["tflops"]
+        return [r["ms"], round(t), round(100 * t / NOMINAL_DENSE_TFLOPS[f], 1),
+                round(100 * t / meas[f], 1), r["tile_quant_eff"]]
+
+    def table(rows, f):
+        return {MODE_KEY.get(m, m): row(r, f) for m, r in rows.items()}
+
+    out = {"cols": "ms,TFLOPS,%nominal,%measured,tile_quant_eff",
+           "nominal_tf": {"bf16": 2250, "fp8": 4500, "mxfp4": 9000},
+           "measured_tf": {k: round(v, 1) for k, v in meas.items()}}
+    cfg = result["config"]
+    out["headline"] = {"workload": cfg["workload"], MODE_KEY[mode]: row(
+        {"ms": result["ms_per_step"], "tflops": result["value"],
+         "tile_quant_eff": cfg["tile_quant_eff"]}, fmt)}
+    ex = result.get("extras")
+    if not ex:
+        return out
+    # the num_sms sweeps first and the per-schedule tables of the headline formats last, so a
+    # log cut from the front keeps the MXFP4 and wave-quantised rows
+    sw = ex.get("num_sms_sweep_persistent", {})
+    if "gemm_bf16_4096" in sw:
+        out["c4_4096_pe"] = {ns: [r["ms"], round(r["tflops"]), r.get("sms_used")]
+                             for ns, r in sw["gemm_bf16_4096"].items()}
+    if "gemm_bf16_skinny_64x14336x4096" in sw:
+        out["c4_skinny_pe_gbs"] = {ns: [r["ms"], round(r["gbs"]), r.get("sms_used")]
+                                   for ns, r in sw["gemm_bf16_skinny_64x14336x4096"].items()}
+    names = [("c0_bf16_256x256x512_f32", "addmm_bf16_256x256x512_f32out", "bf16"),
+             ("bf16_1024x1024x16384", "gemm_bf16_1024x1024x16384", "bf16"),
+             ("fp8_8192", "addmm_fp8_8192", "fp8"),
+             ("c1_bf16_8192", "addmm_bf16_8192", "bf16")]
+    for key, name, f in names:
+        if name in ex:
+            out[key] = table(ex[name], f)
+    wq = ex.get("gemm_bf16_1920x1920x16384", {})
+    if wq:
+        out["c2_1920_tile128"] = table(wq["tile_128x128"], "bf16")
+        out["c2_1920_auto"] = table(wq["auto"], "bf16")
+    if "addmm_mxfp4_8192" in ex:
+        out["c3_mxfp4_8192"] = table(ex["addmm_mxfp4_8192"], "mxfp4")
+    return out
+
+
+def sms_used(pr, mode, num_sms, sm_count, options=None):
+    """Distinct SMs one call ran on, from the kernels' SM-usage record (an untimed call)."""
+    import torch
+    import sm_constrained_persistent_gb300 as sk
+    opts = dict(options or {})
+    plan = sk.sk_plan(FORMAT_CODE[pr.fmt], pr.M, pr.N, pr.K, num_sms, mode, sm_count, opts)
+    ctas = plan.grid * plan.ctas_per_tile
+    record = torch.full((ctas,), -1, dtype=torch.int32, device=pr.device)
+    opts.update(sm_record=record.data_ptr(), sm_record_len=ctas)
+    stream = torch.cuda.current_stream()
+    if pr.call(mode, num_sms, stream.cuda_stream, options=opts) != 0:
+        raise RuntimeError("recorded call failed")
+    torch.cuda.synchronize()
+    if sk.sk_stream_status(stream.cuda_stream) != 0:
+        raise RuntimeError("recorded call reported an error")
+    r = record.cpu().numpy()
+    if (r < 0).any():
+        raise RuntimeError("a CTA did not record its SM")
+    return int(len(np.unique(r)))
 
 
 def _time_modes(pr, modes, sm_count, peak, dist, num_sms=0, options=None, steps=10, warmup=3,
@@ -712,6 +794,10 @@ def extras(prob, sm_count, dist):
             cache[name] = Problem(name, prob.device)
         return cache[name]
 
+    # the 256 x 256 x 512 fp32-output addmm: data-parallel, and Stream-K over 3 CTAs
+    pr = get("addmm_bf16_256x256x512_f32out")
+    out[pr.name] = _time_modes(pr, ["dp"], sm_count, bpeak, dist)
+    out[pr.name]["sk3"] = _time_modes(pr, ["streamk"], sm_count, bpeak, dist, num_sms=3)["streamk"]
     for name in ["addmm_bf16_8192", "addmm_mxfp4_8192", "addmm_fp8_8192",
                  "gemm_bf16_1024x1024x16384"]:
         pr = get(name)
@@ -732,6 +818,7 @@ def extras(prob, sm_count, dist):
             r = _time_modes(pr, ["persistent"], sm_count, bpeak, dist, num_sms=ns,
                             steps=5 if ns < 16 else 10, warmup=2)["persistent"]
             r["tflops_per_sm"] = round(r["tflops"] / ns, 2)
+            r["sms_used"] = sms_used(pr, "persistent", ns, sm_count)
             if "skinny" in name:
                 bytes_moved = sum(t.numel() * t.element_size() for t in pr.dev.values()) + \
                     pr.C.numel() * pr.C.element_size()

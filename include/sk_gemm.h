@@ -138,6 +138,25 @@ sk_status_t sk_gemm_mxfp4(const void* A, const void* A_scale, const void* B,
  *                         region on top of the (tiles mod g) remainder (0 = the remainder only;
  *                         1 = the "two-tile" variant, in which each CTA's Stream-K share is at
  *                         least one whole tile).  Capped at the tiles there are.
+ *   resident_limit:       test control, 0 = off.  Otherwise the co-residency check of Stream-K
+ *                         and hybrid grids takes this as the number of CTAs (one-CTA tiles) or
+ *                         SM pairs (pair tiles) the device can hold at once, in place of the
+ *                         occupancy the device reports; a grid above it is refused with
+ *                         SK_ERR_NOT_CORESIDENT before anything is launched.  It stands in for
+ *                         a device with less room than the planner assumed (the plan itself is
+ *                         not changed), so the refusal can be tested.
+ *   sm_record_len, sm_record:
+ *                         SM-usage record, NULL = off.  Otherwise sm_record is a device buffer
+ *                         of sm_record_len uint32 values (4-byte aligned) and CTA i of the launch
+ *                         writes the index of the SM it runs on (%smid) to sm_record[i] when it
+ *                         starts: one 4-byte store per CTA.  The launch has
+ *                         plan.grid * plan.ctas_per_tile CTAs (sk_plan); a call whose launch
+ *                         has more CTAs than sm_record_len is refused with SK_ERR_INVALID_ARG.
+ *                         The distinct values show how many SMs an SM-constrained call used
+ *                         (flashinfer PR #982 "SM-constraint-GEMM by triton persistent kernel"
+ *                         checks the SMs a capped call occupies in its nsys profile).  Calls
+ *                         that launch several GEMMs (the host-buffer and backward calls) each
+ *                         overwrite the record.
  */
 typedef struct {
   int32_t tile_n;
@@ -147,6 +166,9 @@ typedef struct {
   int32_t drop_release_cta;
   int32_t tile_m;
   int32_t hybrid_sk_waves;
+  int32_t resident_limit;
+  int32_t sm_record_len;
+  void* sm_record;
 } sk_options_t;
 
 sk_status_t sk_gemm_bf16_ex(const void* A, const void* B, const void* bias, void* C,
@@ -246,18 +268,30 @@ sk_status_t sk_addmm_backward_bf16(const void* dC, const void* A, const void* B,
  * its scratch (error words, Stream-K flags and up to 160 partial tiles of 128 x 128 fp32,
  * about 10 MiB) is one fixed array inside the library that every GPU loading the library
  * keeps until the process exits.  Arguments and results are those of sk_gemm_bf16; it
- * always uses 128 x 128 CTA tiles.
+ * always uses 128 x 128 CTA tiles (SK_MODE_AUTO picks the schedule among those tiles only).
  *   - Returns SK_ERR_UNSUPPORTED when the schedule would need more than 160 Stream-K slots.
  *   - The first call on a device looks up the array's device address and prepares the kernel
- *     on that device; make that first call before any stream capture on the device.
+ *     on that device; make that first call before any stream capture on the device.  The
+ *     set-up lasts for the life of the process: do not use this entry point on a device after
+ *     cudaDeviceReset.
  *   - All calls share the one array (it keeps the last call's contents; each call clears the
  *     parts that must start at zero on its stream).  Calls that overlap on the GPU race and
  *     give wrong results: serialise them.
- *   - Kernel-side timeouts of this entry point are not reported by sk_stream_status.
+ *   - Kernel-side timeouts of this entry point are not reported by sk_stream_status; read them
+ *     with sk_gemm_bf16_static_status.
  */
 sk_status_t sk_gemm_bf16_static(const void* A, const void* B, const void* bias, void* C,
                                 sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K,
                                 int num_sms, sk_mode_t mode, void* stream);
+
+/*
+ * sk_gemm_bf16_static_status — waits for `stream`, then returns the error the last
+ * sk_gemm_bf16_static call on the current device recorded (SK_OK, or SK_ERR_TIMEOUT when a
+ * Stream-K wait ran out and its owner left that tile unwritten), or SK_ERR_CUDA if the copy or
+ * the wait fails.  Allocates nothing.  The words are cleared by the next static call, so read
+ * them before it.
+ */
+sk_status_t sk_gemm_bf16_static_status(void* stream);
 
 /*
  * sk_stream_status — waits for `stream`, then returns (and clears) the first error the kernels
@@ -275,6 +309,21 @@ sk_status_t sk_stream_status(void* stream);
  */
 sk_status_t sk_workspace_reserve(int device, void* stream, int max_grid, int64_t max_mx_m,
                                  int64_t max_mx_n, int64_t max_mx_k);
+
+/*
+ * sk_workspace_release — frees the workspace of one (device, stream): its Stream-K slots,
+ * flags, error words and MXFP4 scale scratch, and the device copies, copy streams and events
+ * of the host-buffer calls on that stream.  For callers that create a stream per request, so
+ * that workspaces do not accumulate until sk_workspace_release_all.
+ *   - The frees are queued on `stream` (stream-ordered, no host synchronisation): work already
+ *     queued there still runs with the old buffers.  A later call on the stream creates a new
+ *     workspace.
+ *   - A kernel error recorded in the workspace and not yet read by sk_stream_status is lost.
+ *   - Refused (SK_ERR_UNSUPPORTED) while `stream` is being captured, and when no CUDA device
+ *     is usable.  A (device, stream) with no workspace is not an error.  SK_ERR_INVALID_ARG for
+ *     a device index that does not exist.
+ */
+sk_status_t sk_workspace_release(int device, void* stream);
 
 /* Frees every workspace (synchronises each device that has one first). */
 void sk_workspace_release_all(void);

@@ -36,7 +36,8 @@ class Options(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int32), ("raster_group", ctypes.c_int32),
                 ("spin_timeout_ns", ctypes.c_int64), ("inject_faults", ctypes.c_int32),
                 ("drop_release_cta", ctypes.c_int32), ("tile_m", ctypes.c_int32),
-                ("hybrid_sk_waves", ctypes.c_int32)]
+                ("hybrid_sk_waves", ctypes.c_int32), ("resident_limit", ctypes.c_int32),
+                ("sm_record_len", ctypes.c_int32), ("sm_record", ctypes.c_void_p)]
 
 
 class Plan(ctypes.Structure):
@@ -103,10 +104,14 @@ def lib():
                                                  i32, vp]
             h.sk_gemm_bf16_static.restype = i32
             h.sk_gemm_bf16_static.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, i32, vp]
+            h.sk_gemm_bf16_static_status.restype = i32
+            h.sk_gemm_bf16_static_status.argtypes = [vp]
             h.sk_stream_status.restype = i32
             h.sk_stream_status.argtypes = [vp]
             h.sk_workspace_reserve.restype = i32
             h.sk_workspace_reserve.argtypes = [i32, vp, i32, i64, i64, i64]
+            h.sk_workspace_release.restype = i32
+            h.sk_workspace_release.argtypes = [i32, vp]
             h.sk_workspace_release_all.restype = None
             h.sk_workspace_release_all.argtypes = []
             h.sk_status_string.restype = ctypes.c_char_p
@@ -201,12 +206,21 @@ def sk_gemm_bf16_static(A, B, bias, C, out_dtype, M, N, K, num_sms, mode, stream
     return lib().sk_gemm_bf16_static(A, B, bias, C, out_dtype, M, N, K, num_sms, mode, stream)
 
 
+def sk_gemm_bf16_static_status(stream):
+    """Waits for `stream` and returns the error the last sk_gemm_bf16_static call recorded."""
+    return lib().sk_gemm_bf16_static_status(stream)
+
+
 def sk_stream_status(stream):
     return lib().sk_stream_status(stream)
 
 
 def sk_workspace_reserve(device, stream, max_grid, max_mx_m=0, max_mx_n=0, max_mx_k=0):
     return lib().sk_workspace_reserve(device, stream, max_grid, max_mx_m, max_mx_n, max_mx_k)
+
+
+def sk_workspace_release(device, stream):
+    return lib().sk_workspace_release(device, stream)
 
 
 def sk_workspace_release_all():

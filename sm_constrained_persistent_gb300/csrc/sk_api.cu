@@ -347,7 +347,10 @@ cudaError_t regrow(T** ptr, size_t* have, size_t need, cudaStream_t st) {
   }
   void* p = nullptr;
   cudaError_t e = cudaMallocAsync(&p, need, st);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) {
+    cudaGetLastError();   // an allocation failure must not surface as a later call's launch error
+    return e;
+  }
   *ptr = static_cast<T*>(p);
   *have = need;
   return cudaSuccess;
@@ -357,8 +360,9 @@ cudaError_t regrow(T** ptr, size_t* have, size_t need, cudaStream_t st) {
 sk_status_t ensure_workspace(int dev, cudaStream_t st, size_t P_bytes, size_t flag_count,
                              size_t sf_bytes, Workspace** out, size_t red_bytes = 0) {
   Workspace& w = g_workspaces[{dev, st}];
-  const bool fits = w.err != nullptr && w.P_bytes >= P_bytes && w.flag_count >= flag_count &&
-                    w.sf_bytes >= sf_bytes && w.red_bytes >= red_bytes;
+  const bool fits = w.err != nullptr && w.P_bytes >= P_bytes && w.flags != nullptr &&
+                    w.flag_count >= flag_count && w.sf_bytes >= sf_bytes &&
+                    w.red_bytes >= red_bytes;
   if (!fits) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return SK_ERR_CUDA;
@@ -372,7 +376,10 @@ sk_status_t ensure_workspace(int dev, cudaStream_t st, size_t P_bytes, size_t fl
     if (w.flag_count < flag_count || w.flags == nullptr) {
       size_t bytes = w.flag_count * sizeof(uint32_t);
       const size_t need = std::max<size_t>(flag_count, 1) * sizeof(uint32_t);
-      if (regrow(&w.flags, &bytes, need, st) != cudaSuccess) return SK_ERR_OOM;
+      if (regrow(&w.flags, &bytes, need, st) != cudaSuccess) {
+        w.flag_count = 0;   // the old flags are gone too
+        return SK_ERR_OOM;
+      }
       w.flag_count = bytes / sizeof(uint32_t);
       if (cudaMemsetAsync(w.flags, 0, bytes, st) != cudaSuccess) return SK_ERR_CUDA;
     }
@@ -445,6 +452,10 @@ sk_status_t validate(int format, const void* A, const void* A_scale, const void*
     if (format == 1 && opt->tile_n == 256 && opt->tile_m != 256) return SK_ERR_INVALID_ARG;
     if (opt->spin_timeout_ns < 0 || opt->raster_group < 0 || opt->hybrid_sk_waves < 0)
       return SK_ERR_INVALID_ARG;
+    if (opt->resident_limit < 0 || opt->sm_record_len < 0) return SK_ERR_INVALID_ARG;
+    if (opt->sm_record != nullptr &&
+        (opt->sm_record_len == 0 || (reinterpret_cast<uintptr_t>(opt->sm_record) & 3u) != 0))
+      return SK_ERR_INVALID_ARG;
   }
   return SK_OK;
 }
@@ -505,11 +516,15 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   if ((st = ensure_variant(*di, variant)) != SK_OK) return st;
   const bool streamk = plan.sk_tiles > 0;
   if (streamk) {
-    const int64_t capacity = pair ? di->max_pairs[variant]
-                                  : static_cast<int64_t>(di->ctas_per_sm[variant]) * di->sm_count;
+    int64_t capacity = pair ? di->max_pairs[variant]
+                            : static_cast<int64_t>(di->ctas_per_sm[variant]) * di->sm_count;
+    if (opt != nullptr && opt->resident_limit > 0)
+      capacity = std::min<int64_t>(capacity, opt->resident_limit);
     if (plan.grid > capacity) return SK_ERR_NOT_CORESIDENT;
   }
   const int64_t ctas = static_cast<int64_t>(plan.grid) * plan.ctas_per_tile;
+  if (opt != nullptr && opt->sm_record != nullptr && ctas > opt->sm_record_len)
+    return SK_ERR_INVALID_ARG;
 
   const size_t P_bytes = streamk ? static_cast<size_t>(ctas) * kTileM * plan.tile_n * sizeof(float) : 0;
   const MxLayout mx = mx_layout(plan);
@@ -579,6 +594,7 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   a.flags = ws->flags;
   a.err = ws->err;
   a.c_tma = c_tma ? 1 : 0;
+  a.sm_record = opt != nullptr ? static_cast<uint32_t*>(opt->sm_record) : nullptr;
   a.timeout_ns = static_cast<uint64_t>(
       opt != nullptr && opt->spin_timeout_ns > 0 ? opt->spin_timeout_ns : kDefaultTimeoutNs);
   if (format == 1) {
@@ -755,6 +771,37 @@ sk_status_t sk_workspace_reserve(int device, void* stream_ptr, int max_grid, int
   }
   cudaSetDevice(prev);
   return st;
+}
+
+sk_status_t sk_workspace_release(int device, void* stream_ptr) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream_ptr);
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return SK_ERR_UNSUPPORTED;   // no usable device
+  if (cudaSetDevice(device) != cudaSuccess) return SK_ERR_INVALID_ARG;
+  sk_status_t result = SK_OK;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    result = SK_ERR_CUDA;
+  } else if (cs != cudaStreamCaptureStatusNone) {
+    result = SK_ERR_UNSUPPORTED;
+  } else {
+    {
+      std::lock_guard<std::mutex> lock(g_mutex);
+      const auto it = g_workspaces.find({device, st});
+      if (it != g_workspaces.end()) {
+        // Stream-ordered frees: the buffers go once the work already queued on `st` (the only
+        // stream that uses them) has run, with no host synchronisation.
+        Workspace& w = it->second;
+        void* bufs[] = {w.P, w.flags, w.err, w.sf, w.red};
+        for (void* b : bufs)
+          if (b != nullptr && cudaFreeAsync(b, st) != cudaSuccess) result = SK_ERR_CUDA;
+        g_workspaces.erase(it);
+      }
+    }
+    if (sk::release_host_stage(device, st) != cudaSuccess) result = SK_ERR_CUDA;
+  }
+  cudaSetDevice(prev);
+  return result;
 }
 
 void sk_workspace_release_all(void) {

@@ -52,7 +52,11 @@ bool grow(void** ptr, size_t* have, size_t need, cudaStream_t st) {
     *ptr = nullptr;
     *have = 0;
   }
-  if (cudaMallocAsync(ptr, need, st) != cudaSuccess) return false;
+  if (cudaMallocAsync(ptr, need, st) != cudaSuccess) {
+    cudaGetLastError();   // an allocation failure must not surface as a later call's launch error
+    *ptr = nullptr;
+    return false;
+  }
   *have = need;
   return true;
 }
@@ -216,6 +220,34 @@ sk_status_t run_host(const HostProblem& p, void* stream) {
 }  // namespace
 
 namespace sk {
+
+cudaError_t release_host_stage(int device, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_host_mutex);
+  const auto it = g_stages.find({device, stream});
+  if (it == g_stages.end()) return cudaSuccess;
+  Stage& s = it->second;
+  cudaError_t result = cudaSuccess;
+  // The buffers were grown on `stream`, and every later use of them (the copies on the two copy
+  // streams included) is ordered before the caller's stream resumes, so a free queued on
+  // `stream` runs after all of them.  Streams and events with work pending are destroyed once
+  // that work completes.
+  void* bufs[] = {s.A, s.B, s.bias, s.C, s.A_scale, s.B_scale};
+  for (void* b : bufs)
+    if (b != nullptr && cudaFreeAsync(b, stream) != cudaSuccess) result = cudaErrorUnknown;
+  if (s.h2d != nullptr) {
+    cudaStreamDestroy(s.h2d);
+    cudaStreamDestroy(s.d2h);
+    cudaEventDestroy(s.start);
+    cudaEventDestroy(s.b_ready);
+    cudaEventDestroy(s.done);
+    for (int i = 0; i < kMaxBlocks; ++i) {
+      cudaEventDestroy(s.a_ready[i]);
+      cudaEventDestroy(s.c_ready[i]);
+    }
+  }
+  g_stages.erase(it);
+  return result;
+}
 
 void release_host_stages() {
   std::lock_guard<std::mutex> lock(g_host_mutex);

@@ -427,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int64_t cta = blockIdx.x;
   const Plan& plan = args.plan;
+  record_sm(args.sm_record);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {

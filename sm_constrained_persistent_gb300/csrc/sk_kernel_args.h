@@ -25,6 +25,7 @@ struct Args {
   int64_t sf_kgroups;    // k groups (4 scale blocks = 128 K elements each) per row block
   int32_t c_tma;         // one-CTA kernels: 1 = C is written through the tmC tensor map
   int32_t pad_;
+  uint32_t* sm_record;   // null, or one entry per CTA: the SM it ran on
 };
 
 }  // namespace sk

@@ -217,6 +217,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
   const int64_t pair = blockIdx.x >> 1;
   const int64_t cta = blockIdx.x;
   const Plan& plan = args.plan;
+  record_sm(args.sm_record);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {

@@ -68,6 +68,9 @@ cudaError_t launch_f8(int kind, const Launch& l);
 
 // Frees the device copies, streams and events of the host-buffer entry points.
 void release_host_stages();
+// The same for the host-buffer staging of one (device, stream) only; the device must be
+// current.  Frees are queued on `stream`.
+cudaError_t release_host_stage(int device, cudaStream_t stream);
 
 // Dynamic shared memory of a variant, in bytes.
 size_t variant_smem_bytes(int variant);

@@ -13,6 +13,17 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+
+// Writes the index of this CTA's SM to record[blockIdx.x] (thread 0; no-op for a null record).
+__device__ __forceinline__ void record_sm(uint32_t* record) {
+  if (record != nullptr && threadIdx.x == 0) record[blockIdx.x] = sm_id();
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

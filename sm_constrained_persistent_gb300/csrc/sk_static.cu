@@ -16,13 +16,16 @@
 //    kStaticMaxGrid Stream-K slots.
 //  * On its first call on a device it looks up the array's device address (once per device,
 //    with that device current) and raises the kernel's shared-memory limit; make that first
-//    call before any stream capture on that device.
+//    call before any stream capture on that device.  That set-up is kept for the life of the
+//    process: after a cudaDeviceReset the cached address and limit are stale, so this entry
+//    point must not be used on a device that has been reset.
 //  * Every call on every stream shares the one array, which keeps what the last call left.
 //    Each call clears the error words and the flags (which must start at zero) on its stream
 //    before the GEMM.  Calls that overlap on the GPU (other streams, other host threads) race
 //    on the array and give wrong results: serialise them.
-//  * A kernel-side timeout of this entry point is not reported by sk_stream_status (which
-//    reads the regular workspaces); the owner concerned leaves its tile unwritten.
+//  * A kernel-side timeout is recorded in the array's error words, which each call clears
+//    first; sk_stream_status (which reads the regular workspaces) does not see it, and
+//    sk_gemm_bf16_static_status reads it back.  The owner concerned leaves its tile unwritten.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -119,7 +122,7 @@ extern "C" sk_status_t sk_gemm_bf16_static(const void* A, const void* B, const v
   if (misaligned(A) || misaligned(B) || misaligned(C) || (bias != nullptr && misaligned(bias)))
     return SK_ERR_INVALID_ARG;
   if (out_dtype != SK_F32 && out_dtype != SK_BF16) return SK_ERR_INVALID_ARG;
-  if (mode < SK_MODE_DP || mode > SK_MODE_HYBRID) return SK_ERR_INVALID_ARG;
+  if (mode < SK_MODE_DP || mode > SK_MODE_AUTO) return SK_ERR_INVALID_ARG;
   const int64_t max_dim = (int64_t(1) << 31) - 1;
   if (M < 1 || N < 1 || K < 1 || M > max_dim || N > max_dim || K > max_dim)
     return SK_ERR_INVALID_ARG;
@@ -134,6 +137,7 @@ extern "C" sk_status_t sk_gemm_bf16_static(const void* A, const void* B, const v
   if (st != SK_OK) return st;
 
   sk_options_t opt = {};
+  opt.tile_m = static_cast<int32_t>(kStaticTile);   // SK_MODE_AUTO then picks the schedule only
   opt.tile_n = static_cast<int32_t>(kStaticTile);
   opt.drop_release_cta = -1;
   sk_plan_t plan;
@@ -183,4 +187,24 @@ extern "C" sk_status_t sk_gemm_bf16_static(const void* A, const void* B, const v
   const cudaError_t e = sk::variant_launch(sk::kVariantBf16N128, l);
   if (e == cudaErrorCooperativeLaunchTooLarge) return SK_ERR_NOT_CORESIDENT;
   return e == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+}
+
+extern "C" sk_status_t sk_gemm_bf16_static_status(void* stream_ptr) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SK_ERR_UNSUPPORTED;
+  unsigned char* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (dev < 0 || dev >= kMaxDevices) return SK_ERR_UNSUPPORTED;
+    if (!g_static_devices[dev].ready) return SK_OK;   // no call has run on this device
+    base = g_static_devices[dev].base;
+  }
+  // Ordered after the calls queued on `stream`; the words land in a host variable (no
+  // allocation).
+  uint32_t words[4] = {0, 0, 0, 0};
+  if (cudaMemcpyAsync(words, base, sizeof(words), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return SK_ERR_CUDA;
+  return words[0] == 0 ? SK_OK : static_cast<sk_status_t>(words[0]);
 }

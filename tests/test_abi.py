@@ -35,7 +35,8 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for required in ["sk_gemm_bf16", "sk_gemm_mxfp4", "sk_stream_status", "sk_workspace_reserve",
-                     "sk_workspace_release_all", "sk_status_string", "sk_plan", "sk_plan_segments",
+                     "sk_workspace_release_all", "sk_workspace_release", "sk_status_string",
+                     "sk_plan", "sk_plan_segments",
                      "sk_gemm_bf16_ex", "sk_gemm_mxfp4_ex", "sk_gemm_fp8", "sk_gemm_fp8_ex",
                      "sk_gemm_bf16_host", "sk_gemm_fp8_host", "sk_gemm_mxfp4_host",
                      "sk_autotune"]:
@@ -136,6 +137,46 @@ def test_options_validation(lib):
     assert sk.sk_workspace_reserve(0, None, 0) == sk.SK_ERR_INVALID_ARG
     st = sk.sk_gemm_bf16_ex(P, P, None, P, 1, 64, 64, 64, 0, 3, {"hybrid_sk_waves": -1}, None)
     assert st == sk.SK_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("opts", [
+    {"resident_limit": -1}, {"sm_record_len": -4}, {"sm_record": P, "sm_record_len": 0},
+    {"sm_record": P + 2, "sm_record_len": 64},
+])
+def test_bad_resident_limit_and_sm_record_are_rejected_before_cuda(lib, opts):
+    for fn in (sk.sk_gemm_bf16_ex, sk.sk_gemm_fp8_ex):
+        assert fn(P, P, None, P, 1, 64, 64, 64, 0, 2, opts, None) == sk.SK_ERR_INVALID_ARG
+    st = sk.sk_gemm_mxfp4_ex(P, P, P, P, None, P, 1, 64, 64, 64, 0, 2, opts, None)
+    assert st == sk.SK_ERR_INVALID_ARG
+
+
+def test_options_struct_matches_the_c_layout(tmp_path):
+    """sk_options_t as the binding lays it out (size and field offsets) is the C struct."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    fields = [f[0] for f in sk.Options._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "sk_gemm.h"\n'
+                   "int main(void) {\n"
+                   '  printf("%zu\\n", sizeof(sk_options_t));\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(sk_options_t, {f}));\n' for f in fields)
+                   + "  return 0;\n}\n")
+    exe = str(tmp_path / "layout")
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", exe], check=True)
+    got = [int(x) for x in subprocess.run([exe], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [ctypes.sizeof(sk.Options)] + [getattr(sk.Options, f).offset for f in fields]
+    assert got == want
+
+
+def test_workspace_release_without_a_gpu_is_unsupported_not_a_crash(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert sk.sk_workspace_release(0, None) == sk.SK_ERR_UNSUPPORTED
 
 
 # ---- planning -----------------------------------------------------------------------------
