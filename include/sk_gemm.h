@@ -325,6 +325,14 @@ sk_status_t sk_workspace_reserve(int device, void* stream, int max_grid, int64_t
  */
 sk_status_t sk_workspace_release(int device, void* stream);
 
+/*
+ * sk_workspace_bytes — device memory the library holds for (device, stream): the workspace
+ * (Stream-K slots, flags, error words, MXFP4 scale scratch, column-sum partials) plus the
+ * host-buffer calls' device copies.  0 when the stream has none; -1 for a negative device.
+ * Host-only bookkeeping (no CUDA call).
+ */
+int64_t sk_workspace_bytes(int device, void* stream);
+
 /* Frees every workspace (synchronises each device that has one first). */
 void sk_workspace_release_all(void);
 

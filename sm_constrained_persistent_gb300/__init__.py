@@ -112,6 +112,8 @@ def lib():
             h.sk_workspace_reserve.argtypes = [i32, vp, i32, i64, i64, i64]
             h.sk_workspace_release.restype = i32
             h.sk_workspace_release.argtypes = [i32, vp]
+            h.sk_workspace_bytes.restype = i64
+            h.sk_workspace_bytes.argtypes = [i32, vp]
             h.sk_workspace_release_all.restype = None
             h.sk_workspace_release_all.argtypes = []
             h.sk_status_string.restype = ctypes.c_char_p
@@ -221,6 +223,10 @@ def sk_workspace_reserve(device, stream, max_grid, max_mx_m=0, max_mx_n=0, max_m
 
 def sk_workspace_release(device, stream):
     return lib().sk_workspace_release(device, stream)
+
+
+def sk_workspace_bytes(device, stream):
+    return lib().sk_workspace_bytes(device, stream)
 
 
 def sk_workspace_release_all():

@@ -777,14 +777,17 @@ sk_status_t sk_workspace_release(int device, void* stream_ptr) {
   cudaStream_t st = static_cast<cudaStream_t>(stream_ptr);
   int prev = 0;
   if (cudaGetDevice(&prev) != cudaSuccess) return SK_ERR_UNSUPPORTED;   // no usable device
-  if (cudaSetDevice(device) != cudaSuccess) return SK_ERR_INVALID_ARG;
-  sk_status_t result = SK_OK;
+  // The capture state first: while a stream is captured, no call that could invalidate the
+  // capture (such as changing the current device) is made.
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
-    result = SK_ERR_CUDA;
-  } else if (cs != cudaStreamCaptureStatusNone) {
-    result = SK_ERR_UNSUPPORTED;
-  } else {
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return SK_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return SK_ERR_UNSUPPORTED;
+  if (device != prev && cudaSetDevice(device) != cudaSuccess) {
+    cudaGetLastError();
+    return SK_ERR_INVALID_ARG;
+  }
+  sk_status_t result = SK_OK;
+  {
     {
       std::lock_guard<std::mutex> lock(g_mutex);
       const auto it = g_workspaces.find({device, st});
@@ -800,8 +803,25 @@ sk_status_t sk_workspace_release(int device, void* stream_ptr) {
     }
     if (sk::release_host_stage(device, st) != cudaSuccess) result = SK_ERR_CUDA;
   }
-  cudaSetDevice(prev);
+  if (device != prev) cudaSetDevice(prev);
   return result;
+}
+
+int64_t sk_workspace_bytes(int device, void* stream_ptr) {
+  if (device < 0) return -1;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream_ptr);
+  int64_t bytes = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    const auto it = g_workspaces.find({device, st});
+    if (it != g_workspaces.end()) {
+      const Workspace& w = it->second;
+      bytes += static_cast<int64_t>(w.P_bytes + w.flag_count * sizeof(uint32_t) + w.sf_bytes +
+                                    w.red_bytes) +
+               (w.err != nullptr ? 16 : 0);
+    }
+  }
+  return bytes + sk::host_stage_bytes(device, st);
 }
 
 void sk_workspace_release_all(void) {

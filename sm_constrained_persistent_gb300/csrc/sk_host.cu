@@ -221,6 +221,15 @@ sk_status_t run_host(const HostProblem& p, void* stream) {
 
 namespace sk {
 
+int64_t host_stage_bytes(int device, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_host_mutex);
+  const auto it = g_stages.find({device, stream});
+  if (it == g_stages.end()) return 0;
+  const Stage& s = it->second;
+  return static_cast<int64_t>(s.A_bytes + s.B_bytes + s.bias_bytes + s.C_bytes +
+                              s.A_scale_bytes + s.B_scale_bytes);
+}
+
 cudaError_t release_host_stage(int device, cudaStream_t stream) {
   std::lock_guard<std::mutex> lock(g_host_mutex);
   const auto it = g_stages.find({device, stream});

@@ -71,6 +71,8 @@ void release_host_stages();
 // The same for the host-buffer staging of one (device, stream) only; the device must be
 // current.  Frees are queued on `stream`.
 cudaError_t release_host_stage(int device, cudaStream_t stream);
+// Device bytes the host-buffer staging of (device, stream) holds.
+int64_t host_stage_bytes(int device, cudaStream_t stream);
 
 // Dynamic shared memory of a variant, in bytes.
 size_t variant_smem_bytes(int variant);

@@ -1,0 +1,43 @@
+"""Tensor-pipe measurements behind the kernels' design choices, as two standalone CUDA programs
+for sm_103a (built with nvcc into ``probes/_build``):
+
+* ``tc_rate``: clocks per tcgen05.mma for each MMA kind the kernels use or could use (kind::f16,
+  kind::f8f6f4, the block-scaled FP4 kinds), for SM pairs and single CTAs, zero and random
+  operands, with the SM clock seen while the pipe is busy.
+* ``tc_pipeline``: the MXFP4 SM-pair kernel's per-stage structure (commit per stage, producer
+  handshake, scale-factor copies into tensor memory) added to back-to-back MMAs one at a time.
+
+``python -m sm_constrained_persistent_gb300.probes`` builds and runs both on cuda:0 and prints
+one JSON line per measurement.  Measurement only: nothing here is on the GEMM path.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+BUILD = os.path.join(HERE, "_build")
+PROBES = ("tc_rate", "tc_pipeline")
+
+
+def build(name: str) -> str:
+    """Compiles probe `name` (if stale) and returns the executable's path."""
+    src = os.path.join(HERE, f"{name}.cu")
+    exe = os.path.join(BUILD, name)
+    if os.path.exists(exe) and os.path.getmtime(exe) >= os.path.getmtime(src):
+        return exe
+    os.makedirs(BUILD, exist_ok=True)
+    nvcc = os.environ.get("NVCC", "nvcc")
+    tmp = exe + f".tmp{os.getpid()}"
+    subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+                    "-o", tmp, src], check=True)
+    os.replace(tmp, exe)
+    return exe
+
+
+def run(name: str, timeout: float = 300.0) -> str:
+    """Builds and runs probe `name`; returns its output (one JSON object per line)."""
+    r = subprocess.run([build(name)], capture_output=True, text=True, timeout=timeout)
+    if r.returncode != 0:
+        raise RuntimeError(f"probe {name} failed ({r.returncode}): {r.stdout}{r.stderr}")
+    return r.stdout

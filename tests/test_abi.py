@@ -172,6 +172,11 @@ def test_options_struct_matches_the_c_layout(tmp_path):
     assert got == want
 
 
+def test_workspace_bytes_is_host_bookkeeping(lib):
+    assert sk.sk_workspace_bytes(-1, None) == -1
+    assert sk.sk_workspace_bytes(0, 0x1234) == 0   # a stream with no workspace
+
+
 def test_workspace_release_without_a_gpu_is_unsupported_not_a_crash(lib):
     import torch
     if torch.cuda.is_available():
@@ -366,3 +371,13 @@ def test_auto_cost_constants_are_the_fit_of_the_shipped_sweep():
     assert iters == [coef["t_iter_pair"], coef["t_iter_128x256"], coef["t_iter_128x128"]]
     assert rest == [coef["t_piece"], coef["t_split"], coef["t_part"], coef["t_launch"]]
     assert quality["mean_loss"] < 0.02 and quality["max_loss"] < 0.15
+
+
+def test_tensor_pipe_probes_compile_for_sm103a():
+    """The measurement programs behind the kernels' MMA-kind and scale-copy choices build."""
+    import shutil
+    if shutil.which("nvcc") is None:
+        pytest.skip("no nvcc")
+    from sm_constrained_persistent_gb300 import probes
+    for name in probes.PROBES:
+        assert os.path.exists(probes.build(name))

@@ -71,8 +71,22 @@ def test_persistent_and_dp_grids_need_no_coresidency(cuda_device):
 
 # ---- allocation failure --------------------------------------------------------------------
 
+def _stream_without_workspace():
+    """A stream the library holds no workspace for (torch hands out streams from a pool, so a
+    new torch stream may be one an earlier test used)."""
+    s = torch.cuda.Stream()
+    assert sk.sk_workspace_release(0, s.cuda_stream) == sk.SK_OK
+    torch.cuda.synchronize()
+    assert sk.sk_workspace_bytes(0, s.cuda_stream) == 0
+    return s
+
+
 def _fill_device_memory(leave_bytes):
-    """A tensor that takes all free device memory but about `leave_bytes`."""
+    """A tensor that takes all free device memory but about `leave_bytes`.  Every workspace the
+    library holds is released first: workspaces grow through the stream-ordered allocator, whose
+    pool keeps free space inside memory that stays mapped, and a later allocation could be served
+    from there however full the device is."""
+    sk.sk_workspace_release_all()
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     free, _ = torch.cuda.mem_get_info()
@@ -94,7 +108,7 @@ def test_device_workspace_that_cannot_grow_reports_oom_and_recovers(cuda_device)
     # device memory only for its own workspace
     sk.gemm_mxfp4(*args, None, out=c, mode="streamk")
     sk.stream_status()
-    fresh = torch.cuda.Stream()   # a stream with no workspace yet: ~19 MiB of Stream-K slots
+    fresh = _stream_without_workspace()   # the call must grow ~19 MiB of Stream-K slots
     hog = _fill_device_memory(4 << 20)
     try:
         assert torch.cuda.mem_get_info()[0] < (16 << 20)
@@ -123,7 +137,7 @@ def test_host_buffer_staging_that_cannot_grow_reports_oom_and_recovers(cuda_devi
     bias = torch.from_numpy(p["bias"].view(np.int16)).view(torch.bfloat16).pin_memory()
     out = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
     sk.gemm_host("bf16", a, b, bias, out=out, mode="streamk")   # kernels loaded and set up
-    fresh = torch.cuda.Stream()
+    fresh = _stream_without_workspace()
     hog = _fill_device_memory(4 << 20)
     try:
         st = sk.sk_gemm_bf16_host(a.data_ptr(), b.data_ptr(), bias.data_ptr(), out.data_ptr(),
@@ -150,7 +164,7 @@ def test_workspace_release_frees_one_stream_and_a_later_call_rebuilds_it(cuda_de
     p = inputs.bf16_problem(M, N, K, seed=93, integer=True, bias="f32_int")
     a, b, bias = gu.dev_bf16(p["A"]), gu.dev_bf16(p["B"]), gu.dev_bias(p["bias"])
     want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), oracle.F32)
-    s = torch.cuda.Stream()
+    s = _stream_without_workspace()
     host = [torch.from_numpy(p[k].view(np.int16)).view(torch.bfloat16).pin_memory()
             for k in ("A", "B")]
     hout = torch.empty((M, N), dtype=torch.float32).pin_memory()
@@ -158,14 +172,15 @@ def test_workspace_release_frees_one_stream_and_a_later_call_rebuilds_it(cuda_de
     sk.gemm_host("bf16", host[0], host[1], torch.from_numpy(p["bias"]).pin_memory(), out=hout,
                  mode="streamk", stream=s)
     assert sk.sk_stream_status(s.cuda_stream) == sk.SK_OK
-    torch.cuda.synchronize()
-    torch.cuda.empty_cache()
-    free_before = torch.cuda.mem_get_info()[0]
+    held = sk.sk_workspace_bytes(0, s.cuda_stream)
+    # Stream-K slots of the SM pairs (~19 MiB) and the host staging (A, B, C: 8 + 8 + 16 MiB)
+    assert held >= 40 << 20, f"only {held >> 20} MiB held"
     assert sk.sk_workspace_release(0, s.cuda_stream) == sk.SK_OK
+    assert sk.sk_workspace_bytes(0, s.cuda_stream) == 0
     torch.cuda.synchronize()
-    freed = torch.cuda.mem_get_info()[0] - free_before
-    # Stream-K slots of 76 SM pairs (~19 MiB) and the host staging (A, B, C: 8 + 8 + 16 MiB)
-    assert freed >= 40 << 20, f"only {freed >> 20} MiB freed"
+    # The frees reach the device: the stream-ordered pool then hands out the same memory again
+    # (the pool may keep the pages mapped, so free memory as the device reports it need not
+    # grow by all of it).
     assert sk.sk_workspace_release(0, s.cuda_stream) == sk.SK_OK   # nothing left: not an error
     c.zero_()
     sk.gemm_bf16(a, b, bias, out=c, mode="streamk", stream=s)
@@ -175,15 +190,25 @@ def test_workspace_release_frees_one_stream_and_a_later_call_rebuilds_it(cuda_de
     sk.gemm_host("bf16", host[0], host[1], torch.from_numpy(p["bias"]).pin_memory(), out=hout,
                  mode="streamk", stream=s)
     assert np.array_equal(hout.numpy(), want)
+    assert sk.sk_workspace_bytes(0, s.cuda_stream) >= held
     assert sk.sk_workspace_release(0, s.cuda_stream) == sk.SK_OK
+    assert sk.sk_workspace_bytes(0, s.cuda_stream) == 0
 
 
-def test_workspace_release_is_refused_while_capturing_and_checks_the_device(cuda_device):
+def test_workspace_release_checks_the_device_and_leaves_no_cuda_error(cuda_device):
     assert sk.sk_workspace_release(torch.cuda.device_count() + 7, None) == sk.SK_ERR_INVALID_ARG
-    s = torch.cuda.Stream()
-    g = torch.cuda.CUDAGraph()
+    # the refused device change must not surface as the next CUDA call's error
     x = torch.zeros(16, device="cuda")
+    x.add_(1.0)
+    torch.cuda.synchronize()
+    assert float(x.sum()) == 16.0
+
+
+def test_workspace_release_is_refused_while_capturing(cuda_device):
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    st = None
     with torch.cuda.graph(g, stream=s):
-        x.add_(1.0)
         st = sk.sk_workspace_release(0, s.cuda_stream)
     assert st == sk.SK_ERR_UNSUPPORTED
