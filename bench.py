@@ -748,7 +748,7 @@ def auto_selection(device, sm_count, bpeak, dist):
     the automatic plan's time, the fastest configuration and the ratio."""
     from sm_constrained_persistent_gb300 import inputs
     tiles = {"pair": {"tile_m": 256}, "128x256": {"tile_m": 128, "tile_n": 256},
-             "128x128": {"tile_m": 128, "tile_n": 128}}
+             "128x128": {"tile_m": 128, "tile_n": 128}, "128x96": {"tile_m": 128, "tile_n": 96}}
     res = {}
     for (M, N, K) in AUTO_CHECK_SHAPES:
         name = f"gemm_bf16_{M}x{N}x{K}"
@@ -758,7 +758,7 @@ def auto_selection(device, sm_count, bpeak, dist):
         auto = _time_modes(pr, ["auto"], sm_count, bpeak, dist)["auto"]
         best = None
         for tname, opt in tiles.items():
-            if tname == "pair" and M <= 128:
+            if (tname == "pair" and M <= 128) or (tname == "128x96" and M > 128):
                 continue
             for mode, r in _time_modes(pr, ["dp", "persistent", "streamk", "hybrid"], sm_count,
                                        bpeak, dist, options=opt).items():

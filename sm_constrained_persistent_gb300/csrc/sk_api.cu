@@ -31,23 +31,26 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 sk_status_t auto_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, int sm_count,
-                      int max_pairs, const sk_options_t* opt, sk_plan_t* p);
+                      int max_pairs, const sk_options_t* opt, sk_plan_t* p, int layout);
 
 // max_pairs: how many 2-CTA clusters the device can hold at once (the planner's caller passes
-// sm_count / 2 when it cannot ask the device).
+// sm_count / 2 when it cannot ask the device).  layout: the bf16 operand layout (bit 0 A stored
+// transposed, bit 1 B stored transposed); 96-wide tiles exist for the plain layout only.
 sk_status_t make_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, int mode,
-                      int sm_count, int max_pairs, const sk_options_t* opt, sk_plan_t* p) {
+                      int sm_count, int max_pairs, const sk_options_t* opt, sk_plan_t* p,
+                      int layout = 0) {
   if (mode == SK_MODE_AUTO && p != nullptr)
-    return auto_plan(format, M, N, K, num_sms, sm_count, max_pairs, opt, p);
+    return auto_plan(format, M, N, K, num_sms, sm_count, max_pairs, opt, p, layout);
   if (p == nullptr || format < 0 || format > 2 || mode < 0 || mode > 3 || sm_count < 1)
     return SK_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return SK_ERR_INVALID_ARG;
   int tile_n = opt ? opt->tile_n : 0;
   int tile_m = opt ? opt->tile_m : 0;
-  if (tile_n != 0 && tile_n != 128 && tile_n != 256) return SK_ERR_INVALID_ARG;
+  if (tile_n != 0 && tile_n != 96 && tile_n != 128 && tile_n != 256) return SK_ERR_INVALID_ARG;
   if (tile_m != 0 && tile_m != 128 && tile_m != 256) return SK_ERR_INVALID_ARG;
-  if (tile_m == 256 && tile_n == 128) return SK_ERR_INVALID_ARG;
+  if (tile_m == 256 && (tile_n == 128 || tile_n == 96)) return SK_ERR_INVALID_ARG;
+  if (tile_n == 96 && format != 0) return SK_ERR_INVALID_ARG;   // 96-wide tiles: bf16 only
   if (format == 1 && tile_m != 256 && tile_n == 256) return SK_ERR_INVALID_ARG;
   const int64_t sms = (num_sms <= 0 || num_sms > sm_count) ? sm_count : num_sms;
   const int64_t pairs_avail = std::min<int64_t>(sms / 2, max_pairs);
@@ -56,7 +59,7 @@ sk_status_t make_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, 
   if (tile_m == 256) {
     if (pairs_avail < 1) return SK_ERR_INVALID_ARG;
     pair = true;
-  } else if (tile_m == 128 || tile_n == 128) {
+  } else if (tile_m == 128 || tile_n == 128 || tile_n == 96) {
     pair = false;
   } else {
     // SM pairs halve the operand bytes per FLOP; use them when the tile still has more than
@@ -75,6 +78,17 @@ sk_status_t make_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, 
         // Wide tiles halve the B traffic per FLOP; use them while they still fill every SM.
         const int64_t wide_tiles = ceil_div(M, kTileM) * ceil_div(N, 256);
         tile_n = (N >= 256 && wide_tiles >= sm_count) ? 256 : 128;
+        // One row of tiles (M <= 128) streams B: 96-wide tiles put more SMs on it, but each SM
+        // streams a 96-wide tile's columns ~24 % slower (64-byte rows).  Take them when they need
+        // no more waves than 128-wide tiles, so the extra tiles only add SMs: 64 x 14336 on 152
+        // SMs runs 150 tiles in one wave instead of 112 (31.0 vs 33.1 us); on 32 SMs, 5 waves of
+        // 96-wide tiles took 96 us against 78 us for 4 waves of 128-wide ones.
+        if (format == 0 && layout == 0 && tile_n == 128 && M <= kTileM && N > 96 &&
+            (mode == SK_MODE_DP || mode == SK_MODE_PERSISTENT)) {
+          const int64_t workers = mode == SK_MODE_DP ? sm_count : sms;
+          const int64_t t128 = ceil_div(N, 128), t96 = ceil_div(N, 96);
+          if (ceil_div(t96, workers) <= ceil_div(t128, workers)) tile_n = 96;
+        }
       }
     }
   }
@@ -138,7 +152,10 @@ constexpr double kMxIterScale = 1.45;
 
 double plan_cost(const sk_plan_t& p, int format) {
   const int kind = p.ctas_per_tile == 2 ? 0 : (p.tile_n == 256 ? 1 : 2);
-  const double t_iter = kCost.t_iter[kind] * (format == 1 ? kMxIterScale : 1.0);
+  // A 96-wide k-iteration takes about as long as a 128-wide one on a busy SM (three quarters of
+  // the B bytes at ~76 % of the rate); in one wave on more SMs the whole call ran ~6 % faster.
+  const double t_iter = kCost.t_iter[kind] * (format == 1 ? kMxIterScale : 1.0) *
+                        (p.tile_n == 96 ? 0.94 : 1.0);
   const int64_t g = std::max<int64_t>(p.grid, 1), T = p.tiles, I = p.iters;
   double iters = 0.0, pieces = 0.0, fixup = 0.0;
   if (p.mode == SK_MODE_DP || p.mode == SK_MODE_PERSISTENT) {
@@ -160,9 +177,9 @@ double plan_cost(const sk_plan_t& p, int format) {
 }
 
 sk_status_t auto_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, int sm_count,
-                      int max_pairs, const sk_options_t* opt, sk_plan_t* p) {
+                      int max_pairs, const sk_options_t* opt, sk_plan_t* p, int layout) {
   struct Tile { int m, n; };
-  const Tile tiles[3] = {{256, 256}, {128, 256}, {128, 128}};
+  const Tile tiles[4] = {{256, 256}, {128, 256}, {128, 128}, {128, 96}};
   const int modes[3] = {SK_MODE_PERSISTENT, SK_MODE_STREAMK, SK_MODE_HYBRID};
   sk_options_t base = {};
   base.drop_release_cta = -1;
@@ -178,13 +195,15 @@ sk_status_t auto_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, 
     // GB300 than 256-column ones whatever the k-iteration count says: 64x14336x4096 31 vs
     // 38 us, 128x4096x11008 37 vs 55 us, 96x8192x8192 40 vs 49 us (best schedule of each).
     if (base.tile_n == 0 && M <= 128 && t.m == 128 && t.n == 256) continue;
+    // 96-wide tiles: one row of tiles, bf16 in the plain layout
+    if (t.n == 96 && (format != 0 || layout != 0 || M > 128) && base.tile_n != 96) continue;
     for (int mode : modes) {
       sk_options_t o = base;
       o.tile_m = t.m;
       o.tile_n = t.n;
       sk_plan_t cand;
       const sk_status_t st = make_plan(format, M, N, K, num_sms, mode, sm_count, max_pairs, &o,
-                                       &cand);
+                                       &cand, layout);
       if (st != SK_OK) {
         if (!found) first_error = st;
         continue;
@@ -446,9 +465,12 @@ sk_status_t validate(int format, const void* A, const void* A_scale, const void*
     if (K % 32 != 0) return SK_ERR_INVALID_ARG;
   }
   if (opt != nullptr) {
-    if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256) return SK_ERR_INVALID_ARG;
+    if (opt->tile_n != 0 && opt->tile_n != 96 && opt->tile_n != 128 && opt->tile_n != 256)
+      return SK_ERR_INVALID_ARG;
     if (opt->tile_m != 0 && opt->tile_m != 128 && opt->tile_m != 256) return SK_ERR_INVALID_ARG;
-    if (opt->tile_m == 256 && opt->tile_n == 128) return SK_ERR_INVALID_ARG;
+    if (opt->tile_m == 256 && (opt->tile_n == 128 || opt->tile_n == 96)) return SK_ERR_INVALID_ARG;
+    // 96-wide tiles: bf16 in the plain layout only
+    if (opt->tile_n == 96 && (format != 0 || layout != 0)) return SK_ERR_INVALID_ARG;
     if (format == 1 && opt->tile_n == 256 && opt->tile_m != 256) return SK_ERR_INVALID_ARG;
     if (opt->spin_timeout_ns < 0 || opt->raster_group < 0 || opt->hybrid_sk_waves < 0)
       return SK_ERR_INVALID_ARG;
@@ -504,13 +526,14 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   if ((st = ensure_variant(*di, pair_variant)) != SK_OK) return st;
   sk_plan_t plan;
   if ((st = make_plan(format, M, N, K, num_sms, mode, di->sm_count, di->max_pairs[pair_variant],
-                      opt, &plan)) != SK_OK)
+                      opt, &plan, layout)) != SK_OK)
     return st;
   const bool pair = plan.ctas_per_tile == 2;
   const int variant =
       pair ? pair_variant
       : format == 1 ? sk::kVariantMxN128
       : format == 2 ? sk::variant_of(plan.tile_n == 256 ? sk::kKindF8N256 : sk::kKindF8N128, 0)
+      : plan.tile_n == 96 ? sk::variant_of(sk::kKindBf16N96, 0)
                     : sk::variant_of(plan.tile_n == 256 ? sk::kKindBf16N256 : sk::kKindBf16N128,
                                      layout);
   if ((st = ensure_variant(*di, variant)) != SK_OK) return st;
@@ -548,7 +571,11 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
     ok = ((layout & 1) ? encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, 64, 64)
                        : encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, M, K, 64, kTileM)) &&
          ((layout & 2) ? encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, 64, bt_rows)
-                       : encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, 64, 64));
+          : plan.tile_n == 96
+              // 96-wide tiles: boxes of 32 columns (64-byte rows, 64-byte swizzle)
+              ? encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, 32, 64,
+                          CU_TENSOR_MAP_SWIZZLE_64B)
+              : encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, 64, 64));
   } else if (format == 2) {
     // fp8 as bytes: A M x K (box 128 k x 128 rows), B K x N (box 128 n x 128 k-rows).
     ok = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, M, K, 128, kTileM) &&
@@ -623,6 +650,7 @@ extern "C" {
 sk_status_t sk_gemm_bf16(const void* A, const void* B, const void* bias, void* C,
                          sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
                          sk_mode_t mode, void* stream) {
+  const sk::NvtxRange range("sk_gemm_bf16");
   return run_gemm(0, A, nullptr, B, nullptr, bias, C, out_dtype, M, N, K, num_sms, mode, nullptr,
                   stream);
 }
@@ -630,6 +658,7 @@ sk_status_t sk_gemm_bf16(const void* A, const void* B, const void* bias, void* C
 sk_status_t sk_gemm_bf16_ex(const void* A, const void* B, const void* bias, void* C,
                             sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
                             sk_mode_t mode, const sk_options_t* options, void* stream) {
+  const sk::NvtxRange range("sk_gemm_bf16_ex");
   return run_gemm(0, A, nullptr, B, nullptr, bias, C, out_dtype, M, N, K, num_sms, mode, options,
                   stream);
 }
@@ -638,6 +667,7 @@ sk_status_t sk_gemm_mxfp4(const void* A, const void* A_scale, const void* B,
                           const void* B_scale, const void* bias, void* C, sk_dtype_t out_dtype,
                           int64_t M, int64_t N, int64_t K, int num_sms, sk_mode_t mode,
                           void* stream) {
+  const sk::NvtxRange range("sk_gemm_mxfp4");
   return run_gemm(1, A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sms, mode, nullptr,
                   stream);
 }
@@ -646,6 +676,7 @@ sk_status_t sk_gemm_mxfp4_ex(const void* A, const void* A_scale, const void* B,
                              const void* B_scale, const void* bias, void* C,
                              sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
                              sk_mode_t mode, const sk_options_t* options, void* stream) {
+  const sk::NvtxRange range("sk_gemm_mxfp4_ex");
   return run_gemm(1, A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sms, mode, options,
                   stream);
 }
@@ -653,6 +684,7 @@ sk_status_t sk_gemm_mxfp4_ex(const void* A, const void* A_scale, const void* B,
 sk_status_t sk_gemm_fp8(const void* A, const void* B, const void* bias, void* C,
                         sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
                         sk_mode_t mode, void* stream) {
+  const sk::NvtxRange range("sk_gemm_fp8");
   return run_gemm(2, A, nullptr, B, nullptr, bias, C, out_dtype, M, N, K, num_sms, mode, nullptr,
                   stream);
 }
@@ -660,6 +692,7 @@ sk_status_t sk_gemm_fp8(const void* A, const void* B, const void* bias, void* C,
 sk_status_t sk_gemm_fp8_ex(const void* A, const void* B, const void* bias, void* C,
                            sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
                            sk_mode_t mode, const sk_options_t* options, void* stream) {
+  const sk::NvtxRange range("sk_gemm_fp8_ex");
   return run_gemm(2, A, nullptr, B, nullptr, bias, C, out_dtype, M, N, K, num_sms, mode, options,
                   stream);
 }
@@ -668,6 +701,7 @@ sk_status_t sk_gemm_bf16_t(const void* A, int trans_a, const void* B, int trans_
                            const void* bias, void* C, sk_dtype_t out_dtype, int64_t M, int64_t N,
                            int64_t K, int num_sms, sk_mode_t mode, const sk_options_t* options,
                            void* stream) {
+  const sk::NvtxRange range("sk_gemm_bf16_t");
   if ((trans_a != 0 && trans_a != 1) || (trans_b != 0 && trans_b != 1)) return SK_ERR_INVALID_ARG;
   return run_gemm(0, A, nullptr, B, nullptr, bias, C, out_dtype, M, N, K, num_sms, mode, options,
                   stream, trans_a | (trans_b << 1));
@@ -677,6 +711,7 @@ sk_status_t sk_addmm_backward_bf16(const void* dC, const void* A, const void* B,
                                    void* dB, void* dbias, sk_dtype_t grad_dtype, int64_t M,
                                    int64_t N, int64_t K, int num_sms, sk_mode_t mode,
                                    void* stream) {
+  const sk::NvtxRange range("sk_addmm_backward_bf16");
   if (dC == nullptr || (dA == nullptr && dB == nullptr && dbias == nullptr))
     return SK_ERR_INVALID_ARG;
   if ((dA != nullptr && B == nullptr) || (dB != nullptr && A == nullptr)) return SK_ERR_INVALID_ARG;
@@ -719,6 +754,7 @@ sk_status_t sk_addmm_backward_bf16(const void* dC, const void* A, const void* B,
 }
 
 sk_status_t sk_stream_status(void* stream_ptr) {
+  const sk::NvtxRange range("sk_stream_status");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   if (cudaStreamSynchronize(stream) != cudaSuccess) return SK_ERR_CUDA;
   int dev = 0;
@@ -743,6 +779,7 @@ sk_status_t sk_stream_status(void* stream_ptr) {
 
 sk_status_t sk_workspace_reserve(int device, void* stream_ptr, int max_grid, int64_t max_mx_m,
                                  int64_t max_mx_n, int64_t max_mx_k) {
+  const sk::NvtxRange range("sk_workspace_reserve");
   if (max_grid < 1 || max_mx_m < 0 || max_mx_n < 0 || max_mx_k < 0 || (max_mx_k % 32) != 0)
     return SK_ERR_INVALID_ARG;
   int prev = 0;
@@ -774,6 +811,7 @@ sk_status_t sk_workspace_reserve(int device, void* stream_ptr, int max_grid, int
 }
 
 sk_status_t sk_workspace_release(int device, void* stream_ptr) {
+  const sk::NvtxRange range("sk_workspace_release");
   cudaStream_t st = static_cast<cudaStream_t>(stream_ptr);
   int prev = 0;
   if (cudaGetDevice(&prev) != cudaSuccess) return SK_ERR_UNSUPPORTED;   // no usable device
@@ -903,6 +941,7 @@ sk_status_t sk_autotune(int format, const void* A, const void* A_scale, const vo
                         const void* B_scale, const void* bias, void* C, sk_dtype_t out_dtype,
                         int64_t M, int64_t N, int64_t K, int num_sms, int reps, sk_plan_t* chosen,
                         float* best_ms, void* stream_ptr) {
+  const sk::NvtxRange range("sk_autotune");
   if (format < 0 || format > 2 || reps < 1 || reps > 1000) return SK_ERR_INVALID_ARG;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -921,7 +960,7 @@ sk_status_t sk_autotune(int format, const void* A, const void* A_scale, const vo
       {128, 256, SK_MODE_PERSISTENT, 0}, {128, 256, SK_MODE_STREAMK, 0},
       {128, 256, SK_MODE_HYBRID, 0},     {128, 128, SK_MODE_PERSISTENT, 0},
       {128, 128, SK_MODE_STREAMK, 0},    {128, 128, SK_MODE_HYBRID, 0},
-      {128, 128, SK_MODE_HYBRID, 1}};
+      {128, 128, SK_MODE_HYBRID, 1},     {128, 96, SK_MODE_PERSISTENT, 0}};
   auto run = [&](const Cand& c) -> sk_status_t {
     sk_options_t o = {};
     o.drop_release_cta = -1;

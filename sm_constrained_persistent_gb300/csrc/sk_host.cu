@@ -292,6 +292,7 @@ extern "C" {
 sk_status_t sk_gemm_bf16_host(const void* A, const void* B, const void* bias, void* C,
                               sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
                               sk_mode_t mode, const sk_options_t* options, void* stream) {
+  const sk::NvtxRange range("sk_gemm_bf16_host");
   const HostProblem p = {0, A, nullptr, B, nullptr, bias, C, out_dtype, M, N, K, num_sms, mode,
                          options};
   return run_host(p, stream);
@@ -300,6 +301,7 @@ sk_status_t sk_gemm_bf16_host(const void* A, const void* B, const void* bias, vo
 sk_status_t sk_gemm_fp8_host(const void* A, const void* B, const void* bias, void* C,
                              sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K, int num_sms,
                              sk_mode_t mode, const sk_options_t* options, void* stream) {
+  const sk::NvtxRange range("sk_gemm_fp8_host");
   const HostProblem p = {2, A, nullptr, B, nullptr, bias, C, out_dtype, M, N, K, num_sms, mode,
                          options};
   return run_host(p, stream);
@@ -310,6 +312,7 @@ sk_status_t sk_gemm_mxfp4_host(const void* A, const void* A_scale, const void* B
                                sk_dtype_t out_dtype, int64_t M, int64_t N, int64_t K,
                                int num_sms, sk_mode_t mode, const sk_options_t* options,
                                void* stream) {
+  const sk::NvtxRange range("sk_gemm_mxfp4_host");
   const HostProblem p = {1, A, A_scale, B, B_scale, bias, C, out_dtype, M, N, K, num_sms, mode,
                          options};
   return run_host(p, stream);

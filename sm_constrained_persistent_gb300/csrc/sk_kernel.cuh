@@ -57,7 +57,8 @@ enum : uint32_t {
 // (N x K row-major) and read K-major.  kF8: 1-byte E4M3 operands instead of bf16 (same layouts).
 template <bool kMx, int kBN, bool kAT = false, bool kBT = false, bool kF8 = false>
 struct Cfg {
-  static_assert(kBN == 128 || kBN == 256, "tile width");
+  static_assert(kBN == 96 || kBN == 128 || kBN == 256, "tile width");
+  static_assert(kBN != 96 || (!kMx && !kF8 && !kAT && !kBT), "96-wide tiles: bf16, plain layouts");
   static_assert(!kMx || (!kAT && !kBT && !kF8), "MXFP4 operands are K-major");
   static_assert(!kMx || kBN == 128, "MXFP4 tiles are 128 wide");
   // One k-iteration is one 128-byte swizzle row of K: 64 bf16, 128 fp8 or 256 fp4 elements.
@@ -69,13 +70,20 @@ struct Cfg {
   static constexpr int kAtom = kF8 ? 128 : 64;
   static constexpr int kBoxBytes = kTileK * 128;
   static constexpr int kMnAdvance = kMmaK * 128;
+  // B (MN-major) is read in blocks of kAtomB columns with kRowB-byte rows: the 128-byte
+  // blocks above, or for 96-wide tiles three blocks of 32 bf16 (64-byte rows, 64-byte swizzle).
+  static constexpr int kAtomB = kBN == 96 ? 32 : kAtom;
+  static constexpr int kRowB = kBN == 96 ? 64 : 128;
+  static constexpr int kBoxBytesB = kTileK * kRowB;
+  static constexpr uint32_t kLayoutB = kBN == 96 ? kLayoutSwizzle64B : kLayoutSwizzle128B;
   static constexpr int kStageA = kBM * 128;
   static constexpr int kStageB = kBN * 128;
   static constexpr int kStageSfa = kMx ? 1024 : 0;               // 2 k groups x 512 B
   static constexpr int kStageSfb = kMx ? (kBN / 128) * 1024 : 0;
-  static constexpr int kStages = (192 * 1024) / (kStageA + kStageB);
+  // 96-wide tiles stream B for one row of tiles: a deeper ring keeps more of it in flight.
+  static constexpr int kStages = ((kBN == 96 ? 200 : 192) * 1024) / (kStageA + kStageB);
   static constexpr int kStageBytes = kStageA + kStageB + kStageSfa + kStageSfb;
-  static constexpr uint32_t kAccCols = kBN;
+  static constexpr uint32_t kAccCols = kBN == 96 ? 128 : kBN;   // tensor-memory columns per accumulator
   static constexpr uint32_t kSfaCols = 8;              // per stage: 2 groups x 4 columns
   static constexpr uint32_t kSfbCols = 2 * (kBN / 32); // per stage: 2 groups x BN/32 columns
   static constexpr uint32_t kTmemCols = 512;
@@ -498,13 +506,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               tma_load_2d(sa, &tmA, &full[stage], k * TK, tm * kBM);
             }
-            // B: MN-major (TK k-rows x BN n, AT-wide boxes), or K-major (BN rows x TK k).
+            // B: MN-major (TK k-rows x BN n, kAtomB-wide boxes), or K-major (BN rows x TK k).
             if constexpr (kBT) {
               tma_load_2d(sb, &tmB, &full[stage], k * TK, tn * kBN);
             } else {
+              constexpr int ATB = Cf::kAtomB, BXB = Cf::kBoxBytesB;
 #pragma unroll
-              for (int j = 0; j < kBN / AT; ++j)
-                tma_load_2d(sb + j * BX, &tmB, &full[stage], tn * kBN + j * AT, k * TK);
+              for (int j = 0; j < kBN / ATB; ++j)
+                tma_load_2d(sb + j * BXB, &tmB, &full[stage], tn * kBN + j * ATB, k * TK);
             }
           }
           ++issued;
@@ -587,8 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               constexpr uint32_t BX = Cf::kBoxBytes, ADV = Cf::kMnAdvance;
               const uint64_t ad = kAT ? smem_desc(a0 + j * ADV, BX, 1024, kLayoutSwizzle128B)
                                       : smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
+              // MN-major B: blocks kBoxBytesB apart, 8-row K groups 8 * kRowB apart, K advances
+              // kMmaK rows.
+              constexpr uint32_t BXB = Cf::kBoxBytesB, RB = Cf::kRowB;
               const uint64_t bd = kBT ? smem_desc(b0 + j * 32, 16, 1024, kLayoutSwizzle128B)
-                                      : smem_desc(b0 + j * ADV, BX, 1024, kLayoutSwizzle128B);
+                                      : smem_desc(b0 + j * Cf::kMmaK * RB, BXB, 8 * RB, Cf::kLayoutB);
               if constexpr (kF8) {
                 mma_f8(d_tmem, ad, bd, Cf::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
               } else {
@@ -678,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             flag_status = kUnitSkip;
             break;
           }
-          stage_partial<kBN / 32, 2>(
+          stage_partial<kBN / 32, (kBN / 32) % 2 == 0 ? 2 : 1>(
               reinterpret_cast<const float4*>(args.P + (cta + 1 + c) * (kBM * kBN)) + row, t_stage,
               i == 0);
           n_staged = i + 1;

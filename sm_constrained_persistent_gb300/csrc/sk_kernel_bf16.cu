@@ -1,13 +1,13 @@
-// bf16 instantiations of the one-CTA-per-tile GEMM kernel, 128 x 128 tiles, all four
-// operand layouts.
+// bf16 instantiations of the one-CTA-per-tile GEMM kernel: 128 x 128 tiles in all four operand
+// layouts, and 128 x 96 tiles in the plain layout.
 #include "sk_kernel.cuh"
 #include "sk_launch.h"
 
 namespace sk {
 
-template <bool kAT, bool kBT>
+template <bool kAT, bool kBT, int kBN = 128>
 static cudaError_t launch_one(const Launch& l) {
-  using Cf = Cfg<false, 128, kAT, kBT>;
+  using Cf = Cfg<false, kBN, kAT, kBT>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(l.grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -18,20 +18,23 @@ static cudaError_t launch_one(const Launch& l) {
   attr[0].val.cooperative = l.cooperative ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<false, 128, kAT, kBT>, *l.tmA, *l.tmB,
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<false, kBN, kAT, kBT>, *l.tmA, *l.tmB,
                             l.tmC != nullptr ? *l.tmC : *l.tmA, l.args);
 }
 
-template <bool kAT, bool kBT>
+template <bool kAT, bool kBT, int kBN = 128>
 static cudaError_t setup_one(int* ctas_per_sm) {
-  using Cf = Cfg<false, 128, kAT, kBT>;
-  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<false, 128, kAT, kBT>,
+  using Cf = Cfg<false, kBN, kAT, kBT>;
+  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<false, kBN, kAT, kBT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cf::kSmemBytes));
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gemm_kernel<false, 128, kAT, kBT>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gemm_kernel<false, kBN, kAT, kBT>,
                                                        kThreads, Cf::kSmemBytes);
 }
+
+cudaError_t setup_bf16_n96(int* ctas_per_sm) { return setup_one<false, false, 96>(ctas_per_sm); }
+cudaError_t launch_bf16_n96(const Launch& l) { return launch_one<false, false, 96>(l); }
 
 cudaError_t setup_bf16_n128(int layout, int* ctas_per_sm) {
   switch (layout) {

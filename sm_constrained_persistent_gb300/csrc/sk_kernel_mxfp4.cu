@@ -55,6 +55,7 @@ size_t variant_smem_bytes(int variant) {
     case kKindF8N128: return Cfg<false, 128, false, false, true>::kSmemBytes;
     case kKindF8N256: return Cfg<false, 256, false, false, true>::kSmemBytes;
     case kKindF8Pair: return PairCfg<false, false, false, true>::kSmemBytes;
+    case kKindBf16N96: return Cfg<false, 96>::kSmemBytes;
     default: return PairCfg<true>::kSmemBytes;
   }
 }
@@ -75,6 +76,7 @@ cudaError_t variant_setup(int variant, int* ctas_per_sm) {
     }
     case kKindF8N128:
     case kKindF8N256: return setup_f8(variant_kind(variant), ctas_per_sm);
+    case kKindBf16N96: return setup_bf16_n96(ctas_per_sm);
     default: return cudaErrorInvalidValue;   // pair kinds: pair_variant_setup
   }
 }
@@ -101,6 +103,7 @@ cudaError_t variant_launch(int variant, const Launch& l) {
     }
     case kKindF8N128:
     case kKindF8N256: return launch_f8(variant_kind(variant), l);
+    case kKindBf16N96: return launch_bf16_n96(l);
     default: return cudaErrorInvalidValue;   // pair kinds: pair_variant_launch
   }
 }

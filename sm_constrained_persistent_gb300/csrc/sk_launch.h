@@ -3,10 +3,20 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "sk_kernel_args.h"
 
 namespace sk {
+
+// A named NVTX range around one C-ABI call, so a profiler's timeline attributes the kernels to
+// the call that queued them (nearly free when no profiler is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Kernel variants: kernel kind (operand format x CTA tile) x operand layout.  The pair kinds
 // run 2-CTA clusters on 256 x 256 tiles (one CTA per 128 rows); `Launch::grid` always counts
@@ -21,7 +31,8 @@ enum Kind : int {
   kKindF8N128 = 5,     // fp8 (E4M3) kinds: plain layout only
   kKindF8N256 = 6,
   kKindF8Pair = 7,
-  kNumKinds = 8
+  kKindBf16N96 = 8,    // 96-wide bf16 tiles (one row of tiles streaming B): plain layout only
+  kNumKinds = 9
 };
 constexpr int kNumLayouts = 4;
 constexpr int kNumVariants = kNumKinds * kNumLayouts;
@@ -59,6 +70,8 @@ cudaError_t setup_bf16_n128(int layout, int* ctas_per_sm);
 cudaError_t launch_bf16_n128(int layout, const Launch& l);
 cudaError_t setup_bf16_n256(int layout, int* ctas_per_sm);
 cudaError_t launch_bf16_n256(int layout, const Launch& l);
+cudaError_t setup_bf16_n96(int* ctas_per_sm);
+cudaError_t launch_bf16_n96(const Launch& l);
 cudaError_t setup_bf16_pair(int layout, int* max_clusters);
 cudaError_t launch_bf16_pair(int layout, const Launch& l);
 cudaError_t setup_mx_pair(int* max_clusters);

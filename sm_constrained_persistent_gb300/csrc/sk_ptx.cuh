@@ -273,6 +273,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 
 constexpr uint32_t kLayoutSwizzleNone = 0;
 constexpr uint32_t kLayoutSwizzle128B = 2;
+constexpr uint32_t kLayoutSwizzle64B = 4;
 
 // ---- cross-CTA flags (Stream-K fixup) ------------------------------------------------------
 

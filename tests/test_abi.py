@@ -218,10 +218,13 @@ def test_auto_mode_picks_a_concrete_plan_from_the_cost_model():
         assert p.mode in (1, 2, 3)
         rows = sk.sk_plan_segments(p)          # a concrete plan: its segments cover every tile
         assert rows[:, 3].sum() - rows[:, 2].sum() == p.tiles * p.iters
-    # one row of tiles streams B through 128-column tiles, unless a tile is forced
+    # one row of tiles streams B through narrow tiles, unless a tile is forced: 128 or 96
+    # columns (96 where they put more SMs on B in one wave)
     for (M, N, K) in [(96, 8192, 8192), (64, 14336, 4096), (128, 4096, 11008), (1, 4096, 4096)]:
         p = sk.sk_plan(0, M, N, K, 0, "auto", 152)
-        assert (p.tile_m, p.tile_n) == (128, 128), (M, N, K)
+        assert p.tile_m == 128 and p.tile_n in (96, 128), (M, N, K)
+    p = sk.sk_plan(0, 64, 14336, 4096, 0, "auto", 152)
+    assert (p.tile_n, p.mode, p.grid) == (96, 1, 150)
     p = sk.sk_plan(0, 96, 8192, 8192, 0, "auto", 152, {"tile_n": 256})
     assert (p.tile_m, p.tile_n) == (128, 256)
     p = sk.sk_plan(2, 96, 8192, 8192, 0, "auto", 152)        # fp8 follows the same rule
@@ -235,6 +238,28 @@ def test_auto_mode_picks_a_concrete_plan_from_the_cost_model():
     # one SM: no pairs, and still a plan
     p = sk.sk_plan(0, 4096, 4096, 4096, 1, "auto", 152)
     assert p.ctas_per_tile == 1 and p.grid == 1
+
+
+def test_96_wide_tiles_where_they_put_more_sms_on_one_row_of_tiles():
+    # 64 x 14336: 150 tiles of 96 in one wave instead of 112 of 128 on all SMs; not where they
+    # add a wave (1, 16, 32, 64 or 128 SMs)
+    for ns, want in [(0, 96), (151, 96), (150, 96), (149, 128), (32, 128), (16, 128), (64, 128),
+                     (128, 128), (1, 128)]:
+        for mode in ("persistent", "dp"):
+            p = sk.sk_plan(0, 64, 14336, 4096, ns, mode, 152)
+            assert p.tile_n == (want if mode == "persistent" or ns == 0 else p.tile_n), (ns, mode)
+    assert sk.sk_plan(0, 64, 14336, 4096, 0, "dp", 152).tile_n == 96
+    # Stream-K and hybrid, more than one row of tiles, fp8 and MXFP4 keep 128-wide tiles
+    assert sk.sk_plan(0, 64, 14336, 4096, 0, "streamk", 152).tile_n == 128
+    assert sk.sk_plan(0, 256, 14336, 4096, 0, "persistent", 152, {"tile_m": 128}).tile_n == 128
+    assert sk.sk_plan(2, 64, 14336, 4096, 0, "persistent", 152).tile_n == 128
+    assert sk.sk_plan(1, 64, 14336, 4096, 0, "persistent", 152).tile_n == 128
+    # forced, and refused where the kernel does not exist
+    p = sk.sk_plan(0, 1000, 1000, 64, 0, "streamk", 152, {"tile_n": 96})
+    assert (p.tile_m, p.tile_n, p.tiles_n) == (128, 96, 11)
+    for fmt, opts in [(1, {"tile_n": 96}), (2, {"tile_n": 96}), (0, {"tile_m": 256, "tile_n": 96})]:
+        with pytest.raises(sk.SkError):
+            sk.sk_plan(fmt, 1024, 1024, 1024, 0, "persistent", 152, opts)
 
 
 def test_pair_plans():

@@ -354,3 +354,44 @@ def test_streamk_fixup_with_many_and_late_contributors_is_bit_exact(mode, shape,
     for _ in range(2):   # the second launch reuses flags the first one's owners cleared
         c = gu.run_bf16(p, out=out, mode=mode, num_sms=num_sms, options=TILES[tile])
         assert np.array_equal(gu.host_bits(c), want_bits)
+
+
+# ---- 96-wide tiles (one row of tiles streaming B over more SMs) -----------------------------
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", [(64, 14336, 512), (128, 96, 64), (100, 200, 136), (1, 8, 8),
+                                   (128, 1000, 1024), (300, 776, 520)])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_96_wide_tiles_integer_inputs_are_bit_exact(mode, shape, out):
+    M, N, K = shape
+    p = inputs.bf16_problem(M, N, K, seed=M + 3 * N + 5 * K, integer=True,
+                            bias="bf16_int" if out == "bf16" else "f32_int")
+    c = gu.run_bf16(p, out=out, mode=mode, num_sms=37, options={"tile_m": 128, "tile_n": 96})
+    want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]),
+                               oracle.BF16 if out == "bf16" else oracle.F32)
+    assert np.array_equal(gu.host_bits(c), want.view(np.uint16 if out == "bf16" else np.uint32))
+
+
+@pytest.mark.parametrize("mode", ["persistent", "streamk", "hybrid"])
+def test_96_wide_tiles_skinny_shape_matches_oracle(mode):
+    p = inputs.workload("gemm_bf16_skinny_64x14336x4096")
+    c = gu.run_bf16(p, out="bf16", mode=mode, options={"tile_m": 128, "tile_n": 96})
+    plan = sk.sk_plan(0, 64, 14336, 4096, 0, mode, torch.cuda.get_device_properties(0).multi_processor_count,
+                      {"tile_m": 128, "tile_n": 96})
+    assert plan.tile_n == 96 and plan.tiles == 150
+    ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "bf16")
+    gu.assert_close(gu.host_values(c), ref, "bf16", f"skinny/{mode}/96")
+
+
+def test_96_wide_tiles_only_for_plain_bf16():
+    a = torch.zeros((128, 128), dtype=torch.bfloat16, device="cuda")
+    c = torch.empty((128, 128), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    opts = {"tile_m": 128, "tile_n": 96}
+    st = sk.sk_gemm_bf16_t(a.data_ptr(), 1, a.data_ptr(), 0, None, c.data_ptr(), sk.SK_BF16,
+                           128, 128, 128, 0, sk.MODES["persistent"], opts, stream)
+    assert st == sk.SK_ERR_INVALID_ARG
+    u = torch.zeros((128, 128), dtype=torch.uint8, device="cuda")
+    st = sk.sk_gemm_fp8_ex(u.data_ptr(), u.data_ptr(), None, c.data_ptr(), sk.SK_BF16, 128, 128,
+                           128, 0, sk.MODES["persistent"], opts, stream)
+    assert st == sk.SK_ERR_INVALID_ARG
