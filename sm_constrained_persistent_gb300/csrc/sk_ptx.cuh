@@ -317,7 +317,12 @@ __device__ __forceinline__ uint32_t flag_acquire(const uint32_t* flag) {
   return v;
 }
 
+// bar.sync is the .aligned barrier: a warp must reach it as a whole.  Callers let one lane wait
+// (for an accumulator, a flag) while the others go straight to the barrier, so the warp is
+// reconverged first; otherwise the barrier counts the warp as arrived when its first lanes do,
+// and the other warps go on before that one lane's wait is over.
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+  __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
