@@ -588,7 +588,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
             }
           }
           if (store) {
-            if (Cf::kTmaStore && args.c_tma) {
+            // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8)
+            if constexpr (Cf::kTmaStore) {
               store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else {
               store_row_chunk(args, m, n_half + ch * 32, w);
@@ -631,7 +632,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
               load_partial8(pp, src, kBM);
               add_partial8(w, pp, false);
             }
-            if (Cf::kTmaStore && args.c_tma) {
+            // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8)
+            if constexpr (Cf::kTmaStore) {
               store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else {
               store_row_chunk(args, m, n_half + ch * 32, w);
@@ -694,7 +696,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
   #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             float(&w)[32] = *reinterpret_cast<float(*)[32]>(&v[ch * 32]);
-            if (Cf::kTmaStore && args.c_tma) {
+            // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8)
+            if constexpr (Cf::kTmaStore) {
               store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else {
               store_row_chunk(args, m, n_half + ch * 32, w);

@@ -62,3 +62,8 @@ def test_mxfp4_streamk_beside_a_copy(cuda_device):
                                                   mode="streamk", num_sms=76, stream=st))
     assert sk.sk_stream_status(s.cuda_stream) == sk.SK_OK
     assert np.array_equal(gu.host_bits(together), gu.host_bits(alone))
+    ms, ns = gu.sample_positions(2048, 2048, n_random=512, n_rows=2, n_cols=2)
+    ref = gu.reference(oracle.addmm_mxfp4_at(p["A"], p["A_scale"], p["B"], p["B_scale"], None, ms, ns),
+                       "f32")
+    got = together[torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda()]
+    gu.assert_close(got.cpu().numpy().astype(np.float64), ref, "f32", "MXFP4 Stream-K co-run")
