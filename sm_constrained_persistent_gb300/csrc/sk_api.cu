@@ -960,7 +960,8 @@ sk_status_t sk_autotune(int format, const void* A, const void* A_scale, const vo
       {128, 256, SK_MODE_PERSISTENT, 0}, {128, 256, SK_MODE_STREAMK, 0},
       {128, 256, SK_MODE_HYBRID, 0},     {128, 128, SK_MODE_PERSISTENT, 0},
       {128, 128, SK_MODE_STREAMK, 0},    {128, 128, SK_MODE_HYBRID, 0},
-      {128, 128, SK_MODE_HYBRID, 1},     {128, 96, SK_MODE_PERSISTENT, 0}};
+      {128, 128, SK_MODE_HYBRID, 1},     {128, 96, SK_MODE_PERSISTENT, 0},
+      {128, 96, SK_MODE_STREAMK, 0}};
   auto run = [&](const Cand& c) -> sk_status_t {
     sk_options_t o = {};
     o.drop_release_cta = -1;
