@@ -157,6 +157,12 @@ sk_status_t sk_gemm_mxfp4(const void* A, const void* A_scale, const void* B,
  *                         checks the SMs a capped call occupies in its nsys profile).  Calls
  *                         that launch several GEMMs (the host-buffer and backward calls) each
  *                         overwrite the record.
+ *   tile_k:               0 = automatic, else the K a pipeline stage carries: bf16 64 or 128,
+ *                         fp8 128, MXFP4 256.  bf16 128 ("tall" stages) exists for one CTA per
+ *                         96- or 128-wide tile, the plain layout and M <= 64; the automatic
+ *                         choice takes it there (TMA streams B faster in 128-row boxes).  Any
+ *                         other value is SK_ERR_INVALID_ARG.
+ *   reserved:             0.
  */
 typedef struct {
   int32_t tile_n;
@@ -169,6 +175,8 @@ typedef struct {
   int32_t resident_limit;
   int32_t sm_record_len;
   void* sm_record;
+  int32_t tile_k;
+  int32_t reserved;   /* 0 */
 } sk_options_t;
 
 sk_status_t sk_gemm_bf16_ex(const void* A, const void* B, const void* bias, void* C,

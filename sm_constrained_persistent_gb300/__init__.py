@@ -37,7 +37,8 @@ class Options(ctypes.Structure):
                 ("spin_timeout_ns", ctypes.c_int64), ("inject_faults", ctypes.c_int32),
                 ("drop_release_cta", ctypes.c_int32), ("tile_m", ctypes.c_int32),
                 ("hybrid_sk_waves", ctypes.c_int32), ("resident_limit", ctypes.c_int32),
-                ("sm_record_len", ctypes.c_int32), ("sm_record", ctypes.c_void_p)]
+                ("sm_record_len", ctypes.c_int32), ("sm_record", ctypes.c_void_p),
+                ("tile_k", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):

@@ -16,7 +16,8 @@ CSRC = os.path.join(_PKG, "csrc")
 INCLUDE = os.path.join(_ROOT, "include")
 LIB_DIR = os.path.join(_PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libskgemm.so")
-SOURCES = ["sk_api.cu", "sk_kernel_bf16.cu", "sk_kernel_bf16_wide.cu", "sk_kernel_mxfp4.cu",
+SOURCES = ["sk_api.cu", "sk_kernel_bf16.cu", "sk_kernel_bf16_wide.cu", "sk_kernel_bf16_tall.cu",
+           "sk_kernel_mxfp4.cu",
            "sk_kernel_pair.cu", "sk_kernel_pair_mx.cu", "sk_kernel_fp8.cu", "sk_reduce.cu",
            "sk_static.cu", "sk_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

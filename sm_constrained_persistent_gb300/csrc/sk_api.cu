@@ -18,6 +18,7 @@ namespace {
 
 constexpr int kTileM = 128;
 constexpr int kBf16TileK = 64;
+constexpr int64_t kTallMaxRows = 64;   // rows of A a tall-stage tile loads
 constexpr int kMxTileK = 256;
 constexpr int kF8TileK = 128;
 constexpr int kDefaultRasterGroup = 16;
@@ -98,6 +99,17 @@ sk_status_t make_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, 
   p->tile_m = tile_m;
   p->tile_n = tile_n;
   p->tile_k = format == 1 ? kMxTileK : (format == 2 ? kF8TileK : kBf16TileK);
+  // bf16 with at most 64 rows of A on one-CTA 96- or 128-wide tiles (plain layout): tall stages
+  // of 128 K, whose 128-row B boxes TMA streams faster than 64-row ones.
+  const bool tall_ok =
+      format == 0 && layout == 0 && !pair && M <= kTallMaxRows && tile_n != 256;
+  const int tile_k = opt ? opt->tile_k : 0;
+  if (tile_k == 0) {
+    if (tall_ok) p->tile_k = 2 * kBf16TileK;
+  } else if (tile_k != p->tile_k) {
+    if (!(tall_ok && tile_k == 2 * kBf16TileK)) return SK_ERR_INVALID_ARG;
+    p->tile_k = tile_k;
+  }
   p->ctas_per_tile = pair ? 2 : 1;
   const int64_t tiles_m = ceil_div(M, tile_m), tiles_n = ceil_div(N, tile_n);
   const int64_t tiles = tiles_m * tiles_n;
@@ -149,13 +161,18 @@ constexpr CostModel kCost = {{0.3048, 0.3358, 0.2516}, 0.7958, 5.3951, 2.2353, 1
 // A k-iteration carries the same operand bytes in every format; an MXFP4 one (plus its scale
 // copies) takes ~1.45 times a bf16 one (8192^3 persistent: 0.44 vs 0.30 us), fp8 the same.
 constexpr double kMxIterScale = 1.45;
+// Per 64 K, a tall stage's time against a 64-K stage's on the same tile (64 x 14336 x 4096 on
+// one GB300: 128-wide tiles 28.9 against 30.2 us, 96-wide 28.9 against 28.9 us).
+constexpr double kTallIterScale = 0.97;
 
 double plan_cost(const sk_plan_t& p, int format) {
   const int kind = p.ctas_per_tile == 2 ? 0 : (p.tile_n == 256 ? 1 : 2);
   // A 96-wide k-iteration takes about as long as a 128-wide one on a busy SM (three quarters of
   // the B bytes at ~76 % of the rate); in one wave on more SMs the whole call ran ~6 % faster.
+  // A tall stage (128 K) carries two 64-K iterations' bytes, streamed faster (kTallIterScale).
   const double t_iter = kCost.t_iter[kind] * (format == 1 ? kMxIterScale : 1.0) *
-                        (p.tile_n == 96 ? 0.94 : 1.0);
+                        (p.tile_n == 96 ? 0.94 : 1.0) *
+                        (format == 0 && p.tile_k == 2 * kBf16TileK ? 2.0 * kTallIterScale : 1.0);
   const int64_t g = std::max<int64_t>(p.grid, 1), T = p.tiles, I = p.iters;
   double iters = 0.0, pieces = 0.0, fixup = 0.0;
   if (p.mode == SK_MODE_DP || p.mode == SK_MODE_PERSISTENT) {
@@ -475,6 +492,9 @@ sk_status_t validate(int format, const void* A, const void* A_scale, const void*
     if (opt->spin_timeout_ns < 0 || opt->raster_group < 0 || opt->hybrid_sk_waves < 0)
       return SK_ERR_INVALID_ARG;
     if (opt->resident_limit < 0 || opt->sm_record_len < 0) return SK_ERR_INVALID_ARG;
+    if ((opt->tile_k != 0 && opt->tile_k != 64 && opt->tile_k != 128 && opt->tile_k != 256) ||
+        opt->reserved != 0)
+      return SK_ERR_INVALID_ARG;
     if (opt->sm_record != nullptr &&
         (opt->sm_record_len == 0 || (reinterpret_cast<uintptr_t>(opt->sm_record) & 3u) != 0))
       return SK_ERR_INVALID_ARG;
@@ -533,6 +553,8 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
       pair ? pair_variant
       : format == 1 ? sk::kVariantMxN128
       : format == 2 ? sk::variant_of(plan.tile_n == 256 ? sk::kKindF8N256 : sk::kKindF8N128, 0)
+      : plan.tile_k == 2 * kBf16TileK
+          ? sk::variant_of(plan.tile_n == 96 ? sk::kKindBf16N96Tall : sk::kKindBf16N128Tall, 0)
       : plan.tile_n == 96 ? sk::variant_of(sk::kKindBf16N96, 0)
                     : sk::variant_of(plan.tile_n == 256 ? sk::kKindBf16N256 : sk::kKindBf16N128,
                                      layout);
@@ -567,15 +589,19 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   if (format == 0) {
     // A: M x K (box 64 k x 128 rows), or stored K x M (box 64 m x 64 k-rows).
     // B: K x N (box 64 n x 64 k-rows), or stored N x K (box 64 k x one CTA's columns).
+    // Tall stages: A in boxes of 64 k x 64 rows, B in boxes 128 k-rows tall.
     const uint32_t bt_rows = pair ? 128u : static_cast<uint32_t>(plan.tile_n);
+    const bool tall = plan.tile_k == 2 * kBf16TileK;
+    const uint32_t b_rows = tall ? 128u : 64u;
     ok = ((layout & 1) ? encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, K, M, 64, 64)
-                       : encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, M, K, 64, kTileM)) &&
+                       : encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, M, K, 64,
+                                   tall ? 64u : static_cast<uint32_t>(kTileM))) &&
          ((layout & 2) ? encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, N, K, 64, bt_rows)
           : plan.tile_n == 96
               // 96-wide tiles: boxes of 32 columns (64-byte rows, 64-byte swizzle)
-              ? encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, 32, 64,
+              ? encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, 32, b_rows,
                           CU_TENSOR_MAP_SWIZZLE_64B)
-              : encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, 64, 64));
+              : encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, K, N, 64, b_rows));
   } else if (format == 2) {
     // fp8 as bytes: A M x K (box 128 k x 128 rows), B K x N (box 128 n x 128 k-rows).
     ok = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, M, K, 128, kTileM) &&

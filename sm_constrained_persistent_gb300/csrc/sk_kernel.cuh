@@ -55,16 +55,30 @@ enum : uint32_t {
 
 // kAT: A is stored transposed (K x M row-major) and read M-major; kBT: B is stored transposed
 // (N x K row-major) and read K-major.  kF8: 1-byte E4M3 operands instead of bf16 (same layouts).
-template <bool kMx, int kBN, bool kAT = false, bool kBT = false, bool kF8 = false>
+// kTall: bf16 with at most 64 rows of A (one row of tiles streaming B): 128 K per stage, so
+// that every B box is 128 k-rows tall, and only A's 64 real rows are loaded.  Streamed alone
+// through TMA, a 4096 x 14336 bf16 B is read at 5.4 TB/s in 64 x 128 boxes against 4.0 TB/s
+// in 64 x 64 ones; inside the GEMM, whose stages wait for their MMAs before they refill, the
+// gain shrinks to 0-4 %.
+template <bool kMx, int kBN, bool kAT = false, bool kBT = false, bool kF8 = false,
+          bool kTall = false>
 struct Cfg {
   static_assert(kBN == 96 || kBN == 128 || kBN == 256, "tile width");
   static_assert(kBN != 96 || (!kMx && !kF8 && !kAT && !kBT), "96-wide tiles: bf16, plain layouts");
   static_assert(!kMx || (!kAT && !kBT && !kF8), "MXFP4 operands are K-major");
   static_assert(!kMx || kBN == 128, "MXFP4 tiles are 128 wide");
-  // One k-iteration is one 128-byte swizzle row of K: 64 bf16, 128 fp8 or 256 fp4 elements.
-  static constexpr int kTileK = kMx ? 256 : (kF8 ? 128 : 64);
+  static_assert(!kTall || (!kMx && !kF8 && !kAT && !kBT && kBN != 256),
+                "tall stages: bf16, plain layouts, 96- or 128-wide tiles");
+  // One k-iteration is one 128-byte swizzle row of K: 64 bf16, 128 fp8 or 256 fp4 elements
+  // (two rows, 128 bf16, for tall stages).
+  static constexpr int kKHalves = kTall ? 2 : 1;   // 128-byte K atoms of A per stage
+  static constexpr int kTileK = kMx ? 256 : (kF8 ? 128 : 64 * kKHalves);
   static constexpr int kMmaK = kMx ? 64 : (kF8 ? 32 : 16);   // K per tcgen05.mma (32 bytes)
-  static constexpr int kMmasPerStage = kTileK / kMmaK;        // 4
+  static constexpr int kMmasPerStage = kTileK / kMmaK;        // 4 (8 for tall stages)
+  // Rows of A a stage holds per K atom.  Tall stages load only 64: the M = 128 MMA then reads
+  // its rows 64-127 from the next 8 KB of the ring (still inside shared memory), and those
+  // accumulator rows lie at m >= M, which is never stored.
+  static constexpr int kARows = kTall ? 64 : kBM;
   // MN-major tiles are blocks of 128 bytes (kAtom elements) x kTileK k-rows, kBoxBytes each;
   // one MMA's K advances kMnAdvance bytes through a block.
   static constexpr int kAtom = kF8 ? 128 : 64;
@@ -76,8 +90,8 @@ struct Cfg {
   static constexpr int kRowB = kBN == 96 ? 64 : 128;
   static constexpr int kBoxBytesB = kTileK * kRowB;
   static constexpr uint32_t kLayoutB = kBN == 96 ? kLayoutSwizzle64B : kLayoutSwizzle128B;
-  static constexpr int kStageA = kBM * 128;
-  static constexpr int kStageB = kBN * 128;
+  static constexpr int kStageA = kARows * 128 * kKHalves;
+  static constexpr int kStageB = kBN * 128 * kKHalves;
   static constexpr int kStageSfa = kMx ? 1024 : 0;               // 2 k groups x 512 B
   static constexpr int kStageSfb = kMx ? (kBN / 128) * 1024 : 0;
   // 96-wide tiles stream B for one row of tiles: a deeper ring keeps more of it in flight.
@@ -406,11 +420,12 @@ __device__ __forceinline__ void store_row_chunk(const Args& a, int64_t m, int64_
   }
 }
 
-template <bool kMx, int kBN, bool kAT = false, bool kBT = false, bool kF8 = false>
+template <bool kMx, int kBN, bool kAT = false, bool kBT = false, bool kF8 = false,
+          bool kTall = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Args args) {
-  using Cf = Cfg<kMx, kBN, kAT, kBT, kF8>;
+  using Cf = Cfg<kMx, kBN, kAT, kBT, kF8, kTall>;
   constexpr int S = Cf::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -504,7 +519,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int j = 0; j < kBM / AT; ++j)
                 tma_load_2d(sa + j * BX, &tmA, &full[stage], tm * kBM + j * AT, k * TK);
             } else {
-              tma_load_2d(sa, &tmA, &full[stage], k * TK, tm * kBM);
+              // one box of kARows rows x 64 k per 128-byte K atom (two for tall stages)
+#pragma unroll
+              for (int h = 0; h < Cf::kKHalves; ++h)
+                tma_load_2d(sa + h * (Cf::kARows * 128), &tmA, &full[stage], k * TK + h * 64,
+                            tm * kBM);
             }
             // B: MN-major (TK k-rows x BN n, kAtomB-wide boxes), or K-major (BN rows x TK k).
             if constexpr (kBT) {
@@ -593,9 +612,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               //    8-row K groups 1024 B apart (stride offset); K advances 16 rows = 2 KB.
               // K-major: K advances 32 bytes along the swizzled row.  M-major A / MN-major B:
               // blocks of 128-byte rows kBoxBytes apart, K advances kMmaK rows.
+              // (Tall stages: MMAs 4-7 read the second K atom, kARows * 128 bytes on.)
               constexpr uint32_t BX = Cf::kBoxBytes, ADV = Cf::kMnAdvance;
-              const uint64_t ad = kAT ? smem_desc(a0 + j * ADV, BX, 1024, kLayoutSwizzle128B)
-                                      : smem_desc(a0 + j * 32, 16, 1024, kLayoutSwizzle128B);
+              const uint64_t ad =
+                  kAT ? smem_desc(a0 + j * ADV, BX, 1024, kLayoutSwizzle128B)
+                      : smem_desc(a0 + (j / 4) * (Cf::kARows * 128) + (j % 4) * 32, 16, 1024,
+                                  kLayoutSwizzle128B);
               // MN-major B: blocks kBoxBytesB apart, 8-row K groups 8 * kRowB apart, K advances
               // kMmaK rows.
               constexpr uint32_t BXB = Cf::kBoxBytesB, RB = Cf::kRowB;

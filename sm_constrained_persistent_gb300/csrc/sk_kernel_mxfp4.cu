@@ -56,6 +56,8 @@ size_t variant_smem_bytes(int variant) {
     case kKindF8N256: return Cfg<false, 256, false, false, true>::kSmemBytes;
     case kKindF8Pair: return PairCfg<false, false, false, true>::kSmemBytes;
     case kKindBf16N96: return Cfg<false, 96>::kSmemBytes;
+    case kKindBf16N128Tall: return tall_smem_bytes(128);
+    case kKindBf16N96Tall: return tall_smem_bytes(96);
     default: return PairCfg<true>::kSmemBytes;
   }
 }
@@ -77,6 +79,8 @@ cudaError_t variant_setup(int variant, int* ctas_per_sm) {
     case kKindF8N128:
     case kKindF8N256: return setup_f8(variant_kind(variant), ctas_per_sm);
     case kKindBf16N96: return setup_bf16_n96(ctas_per_sm);
+    case kKindBf16N128Tall: return setup_bf16_tall(128, ctas_per_sm);
+    case kKindBf16N96Tall: return setup_bf16_tall(96, ctas_per_sm);
     default: return cudaErrorInvalidValue;   // pair kinds: pair_variant_setup
   }
 }
@@ -104,6 +108,8 @@ cudaError_t variant_launch(int variant, const Launch& l) {
     case kKindF8N128:
     case kKindF8N256: return launch_f8(variant_kind(variant), l);
     case kKindBf16N96: return launch_bf16_n96(l);
+    case kKindBf16N128Tall: return launch_bf16_tall(128, l);
+    case kKindBf16N96Tall: return launch_bf16_tall(96, l);
     default: return cudaErrorInvalidValue;   // pair kinds: pair_variant_launch
   }
 }

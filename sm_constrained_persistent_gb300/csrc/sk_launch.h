@@ -32,7 +32,9 @@ enum Kind : int {
   kKindF8N256 = 6,
   kKindF8Pair = 7,
   kKindBf16N96 = 8,    // 96-wide bf16 tiles (one row of tiles streaming B): plain layout only
-  kNumKinds = 9
+  kKindBf16N128Tall = 9,   // bf16, at most 64 rows of A: 128 K per stage (plain layout only)
+  kKindBf16N96Tall = 10,
+  kNumKinds = 11
 };
 constexpr int kNumLayouts = 4;
 constexpr int kNumVariants = kNumKinds * kNumLayouts;
@@ -72,6 +74,10 @@ cudaError_t setup_bf16_n256(int layout, int* ctas_per_sm);
 cudaError_t launch_bf16_n256(int layout, const Launch& l);
 cudaError_t setup_bf16_n96(int* ctas_per_sm);
 cudaError_t launch_bf16_n96(const Launch& l);
+// Tall stages (128 K per stage, 64 rows of A) for 128- or 96-wide tiles (`bn`).
+cudaError_t setup_bf16_tall(int bn, int* ctas_per_sm);
+cudaError_t launch_bf16_tall(int bn, const Launch& l);
+size_t tall_smem_bytes(int bn);
 cudaError_t setup_bf16_pair(int layout, int* max_clusters);
 cudaError_t launch_bf16_pair(int layout, const Launch& l);
 cudaError_t setup_mx_pair(int* max_clusters);

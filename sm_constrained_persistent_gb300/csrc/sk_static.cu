@@ -29,6 +29,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -102,7 +103,13 @@ sk_status_t static_device(int dev, StaticDevice** out) {
     void* base = nullptr;
     if (cudaGetSymbolAddress(&base, g_static_scratch) != cudaSuccess || base == nullptr)
       return SK_ERR_CUDA;
-    if (sk::variant_setup(sk::kVariantBf16N128, &d.ctas_per_sm) != cudaSuccess) return SK_ERR_CUDA;
+    // the 128 x 128 kernel, and its tall-stage form for problems of at most 64 rows (both one
+    // CTA per SM)
+    int tall_ctas = 0;
+    if (sk::variant_setup(sk::kVariantBf16N128, &d.ctas_per_sm) != cudaSuccess ||
+        sk::variant_setup(sk::variant_of(sk::kKindBf16N128Tall, 0), &tall_ctas) != cudaSuccess)
+      return SK_ERR_CUDA;
+    d.ctas_per_sm = std::min(d.ctas_per_sm, tall_ctas);
     d.base = static_cast<unsigned char*>(base);
     d.ready = true;
   }
@@ -151,8 +158,12 @@ extern "C" sk_status_t sk_gemm_bf16_static(const void* A, const void* B, const v
   // The error words and the flags must start at zero; the partial slots need no clearing.
   if (cudaMemsetAsync(d->base, 0, kErrBytes + kFlagBytes, stream) != cudaSuccess) return SK_ERR_CUDA;
 
+  // The planner gives problems of at most 64 rows tall stages (128 K: A boxes of 64 rows, B
+  // boxes of 128 k-rows).
+  const bool tall = plan.tile_k == 128;
   CUtensorMap tmA, tmB;
-  if (!encode_bf16_2d(&tmA, A, M, K, 64, 128) || !encode_bf16_2d(&tmB, B, K, N, 64, 64))
+  if (!encode_bf16_2d(&tmA, A, M, K, 64, tall ? 64 : 128) ||
+      !encode_bf16_2d(&tmB, B, K, N, 64, tall ? 128 : 64))
     return SK_ERR_CUDA;
 
   sk::Launch l = {};
@@ -184,7 +195,8 @@ extern "C" sk_status_t sk_gemm_bf16_static(const void* A, const void* B, const v
   a.flags = reinterpret_cast<uint32_t*>(d->base + kErrBytes);
   a.P = reinterpret_cast<float*>(d->base + kErrBytes + kFlagBytes);
   a.timeout_ns = 2000000000ull;
-  const cudaError_t e = sk::variant_launch(sk::kVariantBf16N128, l);
+  const cudaError_t e =
+      sk::variant_launch(tall ? sk::variant_of(sk::kKindBf16N128Tall, 0) : sk::kVariantBf16N128, l);
   if (e == cudaErrorCooperativeLaunchTooLarge) return SK_ERR_NOT_CORESIDENT;
   return e == cudaSuccess ? SK_OK : SK_ERR_CUDA;
 }

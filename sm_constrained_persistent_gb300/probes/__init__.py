@@ -6,8 +6,14 @@ for sm_103a (built with nvcc into ``probes/_build``):
   operands, with the SM clock seen while the pipe is busy.
 * ``tc_pipeline``: the MXFP4 SM-pair kernel's per-stage structure (commit per stage, producer
   handshake, scale-factor copies into tensor memory) added to back-to-back MMAs one at a time.
+* ``tma_stream``: the read rate of a 4096 x 14336 bf16 matrix (the B operand of the skinny
+  64 x 14336 x 4096 GEMM) streamed through TMA in column strips, per strip width, box shape,
+  ring depth, K split and L2 promotion, with nothing else running.
+* ``host_link``: host <-> device rates between pinned host memory and the GPU for the host-buffer
+  entry points (268 MB in, 134 MB out): copy engines on 1, 2 or 4 streams, and kernels that load
+  or store pinned host memory directly, per grid size, each direction alone and both at once.
 
-``python -m sm_constrained_persistent_gb300.probes`` builds and runs both on cuda:0 and prints
+``python -m sm_constrained_persistent_gb300.probes`` builds and runs them on cuda:0 and prints
 one JSON line per measurement.  Measurement only: nothing here is on the GEMM path.
 """
 from __future__ import annotations
@@ -17,7 +23,7 @@ import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 BUILD = os.path.join(HERE, "_build")
-PROBES = ("tc_rate", "tc_pipeline")
+PROBES = ("tc_rate", "tc_pipeline", "tma_stream", "host_link")
 
 
 def build(name: str) -> str:

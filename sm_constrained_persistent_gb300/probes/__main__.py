@@ -1,4 +1,4 @@
-"""Builds and runs the tensor-pipe probes on cuda:0 (see the package docstring)."""
+"""Builds and runs the measurement probes on cuda:0 (see the package docstring)."""
 import sys
 
 from . import PROBES, run

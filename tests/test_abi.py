@@ -262,6 +262,30 @@ def test_96_wide_tiles_where_they_put_more_sms_on_one_row_of_tiles():
             sk.sk_plan(fmt, 1024, 1024, 1024, 0, "persistent", 152, opts)
 
 
+def test_tall_stages_for_at_most_64_rows_of_a():
+    # bf16, one CTA per 96- or 128-wide tile, plain layout, M <= 64: 128 K per stage
+    for M in (1, 8, 63, 64):
+        for mode, tn in (("persistent", 96), ("streamk", 128), ("dp", 96), ("hybrid", 128)):
+            p = sk.sk_plan(0, M, 14336, 4096, 0, mode, 152)
+            assert (p.tile_m, p.tile_n, p.tile_k, p.iters) == (128, tn, 128, 32), (M, mode)
+    p = sk.sk_plan(0, 64, 14336, 4104, 0, "streamk", 152)
+    assert (p.tile_k, p.iters) == (128, 33)                         # a ragged last stage
+    # more rows of A, 256-wide tiles, pairs, other formats: the usual stages
+    assert sk.sk_plan(0, 65, 14336, 4096, 0, "persistent", 152).tile_k == 64
+    assert sk.sk_plan(0, 64, 14336, 4096, 0, "persistent", 152, {"tile_n": 256}).tile_k == 64
+    assert sk.sk_plan(2, 64, 14336, 4096, 0, "persistent", 152).tile_k == 128   # fp8's own
+    assert sk.sk_plan(1, 64, 14336, 4096, 0, "persistent", 152).tile_k == 256
+    # forced either way where it exists, refused where it does not
+    p = sk.sk_plan(0, 64, 14336, 4096, 0, "persistent", 152, {"tile_k": 64})
+    assert (p.tile_k, p.iters) == (64, 64)
+    assert sk.sk_plan(0, 32, 4096, 4096, 0, "persistent", 152, {"tile_k": 128}).tile_k == 128
+    for fmt, M, opts in [(0, 65, {"tile_k": 128}), (0, 64, {"tile_k": 128, "tile_n": 256}),
+                         (0, 64, {"tile_k": 256}), (2, 64, {"tile_k": 64}),
+                         (1, 64, {"tile_k": 128}), (0, 64, {"tile_k": 96})]:
+        with pytest.raises(sk.SkError):
+            sk.sk_plan(fmt, M, 14336, 4096, 0, "persistent", 152, opts)
+
+
 def test_pair_plans():
     # large problems go to SM pairs: 256 x 256 tiles, grid counted in pairs
     p = sk.sk_plan(0, 8192, 8192, 8192, 0, "streamk", 152)

@@ -290,6 +290,36 @@ def test_at_most_64_rows_random_bf16_output_matches_oracle():
         gu.assert_close(gu.host_values(c), ref, "bf16", mode)
 
 
+# ---- tall stages (128 K per stage) for at most 64 rows of A ----------------------------------
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", [(64, 14336, 4104), (33, 1000, 136), (1, 256, 8), (64, 96, 4096),
+                                   (64, 8, 64), (17, 2000, 1032)])
+@pytest.mark.parametrize("tile_n", [96, 128])
+@pytest.mark.parametrize("num_sms", [0, 7, 37])
+def test_tall_stages_are_bit_exact_and_equal_64k_stages(mode, shape, tile_n, num_sms):
+    M, N, K = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    opts = {"tile_m": 128, "tile_n": tile_n}
+    plan = sk.sk_plan(0, M, N, K, num_sms, mode, sms, opts)
+    assert plan.tile_k == 128 and plan.iters == -(-K // 128)
+    p = inputs.bf16_problem(M, N, K, seed=M + 5 * N + 3 * K + tile_n, integer=True, bias="f32_int")
+    want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), oracle.F32)
+    tall = gu.run_bf16(p, out="f32", mode=mode, num_sms=num_sms, options=opts)
+    assert np.array_equal(gu.host_bits(tall), want.view(np.uint32))
+    short = gu.run_bf16(p, out="f32", mode=mode, num_sms=num_sms, options=dict(opts, tile_k=64))
+    assert np.array_equal(gu.host_bits(short), gu.host_bits(tall))
+
+
+def test_tall_stages_random_bf16_output_matches_oracle():
+    p = inputs.bf16_problem(64, 3000, 8200, seed=21, operand_scale="sqrt_k", bias="bf16_uniform")
+    for mode in MODES:
+        for tile_n in (96, 128):
+            c = gu.run_bf16(p, out="bf16", mode=mode, options={"tile_m": 128, "tile_n": tile_n})
+            ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "bf16")
+            gu.assert_close(gu.host_values(c), ref, "bf16", f"tall/{mode}/{tile_n}")
+
+
 # ---- the two-tile hybrid (full waves added to the Stream-K region) --------------------------
 
 @pytest.mark.parametrize("shape", [(2304, 2304, 1024), (1000, 3000, 640), (520, 776, 1000)])

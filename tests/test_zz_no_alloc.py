@@ -55,6 +55,26 @@ def test_static_scratch_entry_matches_allocating_entry_twice(cuda_device, mode, 
         gu.assert_close(values, ref, out, f"{mode} call {call} against the oracle")
 
 
+@pytest.mark.parametrize("mode", ["streamk", "hybrid", "persistent", "dp"])
+def test_static_scratch_entry_with_tall_stages_is_bit_exact(cuda_device, mode):
+    # at most 64 rows of A: the static entry runs the tall-stage (128 K) kernel too
+    m, n, k = 48, 2056, 4104
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = sk.sk_plan(0, m, n, k, 0, mode, sms, {"tile_m": 128, "tile_n": 128})
+    assert (plan.tile_k, plan.iters) == (128, 33)
+    p = inputs.bf16_problem(m, n, k, seed=77, integer=True, bias="f32_int")
+    want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), oracle.F32)
+    a, b, bias = gu.dev_bf16(p["A"]), gu.dev_bf16(p["B"]), gu.dev_bias(p["bias"])
+    stream = torch.cuda.current_stream().cuda_stream
+    for call in range(2):
+        got = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+        st = sk.sk_gemm_bf16_static(a.data_ptr(), b.data_ptr(), bias.data_ptr(), got.data_ptr(),
+                                    sk.SK_F32, m, n, k, 0, sk.MODES[mode], stream)
+        assert st == sk.SK_OK, sk.STATUS.get(st, st)
+        assert sk.sk_gemm_bf16_static_status(stream) == sk.SK_OK
+        assert np.array_equal(gu.host_bits(got), want.view(np.uint32)), (mode, call)
+
+
 def test_static_scratch_entry_allocates_no_device_memory(cuda_device):
     p, ref = _problem("bf16")
     a, b, bias = gu.dev_bf16(p["A"]), gu.dev_bf16(p["B"]), gu.dev_bias(p["bias"])
