@@ -610,16 +610,18 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
     ok = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, M, K / 2, 128, kTileM) &&
          encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, N, K / 2, 128, b_box);
   }
-  // C leaves through TMA stores of 32 rows x 64 bytes (64-byte swizzle) when its row pitch is a
-  // multiple of 16 bytes: always for bf16 and fp8 operands (N % 8 == 0), and for MXFP4 when N
-  // allows.  The MXFP4 pair kernel has no room for the staging buffers and stores directly.
-  const bool c_tma = (out_dtype == SK_BF16 ? N % 8 == 0 : N % 4 == 0) && !(pair && format == 1);
+  // C leaves through TMA stores when its row pitch is a multiple of 16 bytes: always for bf16
+  // and fp8 operands (N % 8 == 0), and for MXFP4 when N allows.  Boxes of 32 rows x 64 bytes
+  // (64-byte swizzle); the MXFP4 pair kernel, with room for a 1 KB buffer per warp only, stores
+  // 32 rows x 32 bytes at a time (no swizzle).
+  const bool c_tma = out_dtype == SK_BF16 ? N % 8 == 0 : N % 4 == 0;
+  const bool c_small = pair && format == 1;
   if (ok && c_tma) {
+    const uint32_t box_bytes = c_small ? 32u : 64u;
+    const CUtensorMapSwizzle sw = c_small ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B;
     ok = out_dtype == SK_BF16
-             ? encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, M, N, 32, 32,
-                         CU_TENSOR_MAP_SWIZZLE_64B)
-             : encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, M, N, 16, 32,
-                         CU_TENSOR_MAP_SWIZZLE_64B);
+             ? encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, M, N, box_bytes / 2, 32, sw)
+             : encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, M, N, box_bytes / 4, 32, sw);
   }
   if (!ok) return SK_ERR_CUDA;
 

@@ -351,6 +351,49 @@ __device__ __forceinline__ void store_chunk_tma(const Args& a, const CUtensorMap
   }
 }
 
+// The same through one 1 KB staging buffer per warp (the MXFP4 pair kernel's shared memory has
+// room for no more): pieces of 32 bytes of each of the warp's 32 rows -- 16 bf16 or 8 fp32
+// columns, two or four per 32-column chunk -- each stored by TMA (C's tensor map then has
+// 32 x 32-byte boxes, no swizzle) once the previous piece has been read out of the buffer.
+__device__ __forceinline__ void store_chunk_tma_1k(const Args& a, const CUtensorMap* tmC,
+                                                   uint8_t* buf, int lane, int64_t n0, int64_t y,
+                                                   float (&v)[32]) {
+  add_bias_chunk(a, n0, v);
+  const int cols = a.out_bf16 ? 16 : 8;   // columns per 32-byte piece
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    if (a.out_bf16 && p >= 2) break;
+    const int64_t x = n0 + cols * p;
+    if (x >= a.N || y >= a.M) break;
+    uint4 q[2];
+    if (a.out_bf16) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q[i]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          h[e] = __floats2bfloat162_rn(v[16 * p + 8 * i + 2 * e], v[16 * p + 8 * i + 2 * e + 1]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        q[i] = make_uint4(__float_as_uint(v[8 * p + 4 * i]), __float_as_uint(v[8 * p + 4 * i + 1]),
+                          __float_as_uint(v[8 * p + 4 * i + 2]), __float_as_uint(v[8 * p + 4 * i + 3]));
+    }
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+    uint4* dst = reinterpret_cast<uint4*>(buf + lane * 32);
+    dst[0] = q[0];
+    dst[1] = q[1];
+    fence_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmC, buf, static_cast<int32_t>(x), static_cast<int32_t>(y));
+      bulk_commit();
+    }
+  }
+}
+
 // Adds the bias, casts and stores 32 consecutive columns [n0, n0+32) of row m.
 __device__ __forceinline__ void store_row_chunk(const Args& a, int64_t m, int64_t n0,
                                                 float (&v)[32]) {

@@ -157,8 +157,10 @@ struct PairCfg {
   static constexpr int kStages = (212 * 1024) / kStageBytes;
   // bf16 / fp8 results leave through TMA stores: each epilogue warp stages 32 rows x 64 bytes
   // of C in one of its two 2 KB buffers.  (MXFP4 keeps its scale-factor slots instead.)
+  // MXFP4 keeps its scale-factor slots and has room for one 1 KB buffer per warp: its C leaves
+  // through 32 x 32-byte TMA stores when C's rows are 16-byte aligned (args.c_tma).
   static constexpr bool kTmaStore = !kMx;
-  static constexpr int kEpiBytes = kTmaStore ? 8 * 2 * 2048 : 0;
+  static constexpr int kEpiBytes = kTmaStore ? 8 * 2 * 2048 : 8 * 1024;
   static constexpr int kAccBufs = kMx ? 1 : 2;
   static constexpr uint32_t kAccCols = kBN;
   static constexpr uint32_t kSfaCols = 8;
@@ -448,7 +450,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
     int acc = 0;
     uint32_t acc_phase = 0;
     int parity = 0;
-    uint8_t* my_stage = epi_stage + (warp - 2) * 4096;   // this warp's two staging buffers
+    // this warp's staging: two 2 KB buffers (bf16 / fp8), one 1 KB buffer (MXFP4)
+    uint8_t* my_stage = epi_stage + (warp - 2) * (Cf::kEpiBytes / 8);
     int sbuf = 0;
     Cursor cur(plan, pair);
     Unit u;
@@ -591,6 +594,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
             // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8)
             if constexpr (Cf::kTmaStore) {
               store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
+            } else if (args.c_tma) {
+              store_chunk_tma_1k(args, &tmC, my_stage, lane, n_half + ch * 32, y_warp, w);
             } else {
               store_row_chunk(args, m, n_half + ch * 32, w);
             }
@@ -635,6 +640,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
             // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8)
             if constexpr (Cf::kTmaStore) {
               store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
+            } else if (args.c_tma) {
+              store_chunk_tma_1k(args, &tmC, my_stage, lane, n_half + ch * 32, y_warp, w);
             } else {
               store_row_chunk(args, m, n_half + ch * 32, w);
             }
@@ -699,6 +706,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
             // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8)
             if constexpr (Cf::kTmaStore) {
               store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
+            } else if (args.c_tma) {
+              store_chunk_tma_1k(args, &tmC, my_stage, lane, n_half + ch * 32, y_warp, w);
             } else {
               store_row_chunk(args, m, n_half + ch * 32, w);
             }
@@ -711,7 +720,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
         acc_phase ^= 1u;
       }
     }
-    if constexpr (Cf::kTmaStore) {
+    if (Cf::kTmaStore || args.c_tma) {
       if (lane == 0) bulk_wait_all();   // staged pieces are read and written before exit
     }
   }
