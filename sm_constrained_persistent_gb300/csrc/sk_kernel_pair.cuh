@@ -156,9 +156,9 @@ struct PairCfg {
   static constexpr int kStageBytes = kStageA + kStageB + kStageSfa + kStageSfb;
   static constexpr int kStages = (212 * 1024) / kStageBytes;
   // bf16 / fp8 results leave through TMA stores: each epilogue warp stages 32 rows x 64 bytes
-  // of C in one of its two 2 KB buffers.  (MXFP4 keeps its scale-factor slots instead.)
-  // MXFP4 keeps its scale-factor slots and has room for one 1 KB buffer per warp: its C leaves
-  // through 32 x 32-byte TMA stores when C's rows are 16-byte aligned (args.c_tma).
+  // of C in one of its two 2 KB buffers.  MXFP4, whose scale-factor slots take the room, has
+  // one 1 KB buffer per warp: its C leaves through 32 x 32-byte TMA stores when C's rows are
+  // 16-byte aligned (args.c_tma), else through direct stores.
   static constexpr bool kTmaStore = !kMx;
   static constexpr int kEpiBytes = kTmaStore ? 8 * 2 * 2048 : 8 * 1024;
   static constexpr int kAccBufs = kMx ? 1 : 2;
@@ -591,7 +591,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
             }
           }
           if (store) {
-            // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8)
+            // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8);
+            // MXFP4 ones when N allows
             if constexpr (Cf::kTmaStore) {
               store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else if (args.c_tma) {
@@ -637,7 +638,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
               load_partial8(pp, src, kBM);
               add_partial8(w, pp, false);
             }
-            // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8)
+            // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8);
+            // MXFP4 ones when N allows
             if constexpr (Cf::kTmaStore) {
               store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else if (args.c_tma) {
@@ -703,7 +705,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
   #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             float(&w)[32] = *reinterpret_cast<float(*)[32]>(&v[ch * 32]);
-            // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8)
+            // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8);
+            // MXFP4 ones when N allows
             if constexpr (Cf::kTmaStore) {
               store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else if (args.c_tma) {
