@@ -5,40 +5,60 @@
 
 namespace sk {
 
-// One 128-thread block per 512-byte output group (row block rb, k group g): thread t writes
-// word t, i.e. scales (row rb*128 + 32*(t%4) + t/4, blocks 4g .. 4g+3).  blockIdx.y < a_blocks
-// covers A, the rest B.
+// Word of output group (row block, k group g) for row r: scales of blocks 4g .. 4g+3, padding
+// (127, scale 1.0) outside the matrix.
+__device__ __forceinline__ uint32_t scale_word(const uint8_t* __restrict__ s, int32_t r, int32_t rows,
+                                               int32_t kblocks, int32_t g) {
+  const int32_t kb0 = g * 4;
+  if (r < rows && kb0 + 4 <= kblocks && (kblocks & 3) == 0)
+    return __ldg(reinterpret_cast<const uint32_t*>(s + static_cast<int64_t>(r) * kblocks + kb0));
+  uint32_t word = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int32_t kb = kb0 + j;
+    const uint32_t byte = (r < rows && kb < kblocks) ? s[static_cast<int64_t>(r) * kblocks + kb] : 127u;
+    word |= byte << (8 * j);
+  }
+  return word;
+}
+
+// One 128-thread block per row block rb and span of kPrepGroups 512-byte output groups: in
+// group g, thread t writes word t, i.e. the scales of row rb*128 + 32*(t%4) + t/4, blocks 4g ..
+// 4g+3.  Where the span's 32 scale bytes of a row are whole and 16-byte aligned, the thread reads
+// them with two 16-byte loads.  blockIdx.y < a_blocks covers A, the rest B.
+constexpr int kPrepGroups = 8;
+
 __global__ void __launch_bounds__(128) mx_scale_prep_kernel(
     const uint8_t* __restrict__ sa, int32_t a_rows, int32_t a_blocks, const uint8_t* __restrict__ sb,
     int32_t b_rows, int32_t kblocks, int32_t kgroups, uint32_t* __restrict__ out) {
-  const int32_t g = blockIdx.x;
+  const int32_t g0 = blockIdx.x * kPrepGroups;
   int32_t rb = blockIdx.y;
   const bool is_a = rb < a_blocks;
   const uint8_t* s = is_a ? sa : sb;
   const int32_t rows = is_a ? a_rows : b_rows;
   const int32_t t = threadIdx.x;
   const int32_t r = (is_a ? rb : rb - a_blocks) * 128 + (t & 3) * 32 + (t >> 2);
-  const int32_t kb0 = g * 4;
-  uint32_t word;
-  if (r < rows && kb0 + 4 <= kblocks && (kblocks & 3) == 0) {
-    word = __ldg(reinterpret_cast<const uint32_t*>(s + static_cast<int64_t>(r) * kblocks + kb0));
-  } else {
-    word = 0;
+  uint32_t* dst = out + (static_cast<int64_t>(rb) * kgroups + g0) * 128 + t;
+  const uint8_t* src = s + static_cast<int64_t>(r) * kblocks + g0 * 4;
+  const bool whole = r < rows && (kblocks & 15) == 0 && g0 * 4 + 4 * kPrepGroups <= kblocks &&
+                     g0 + kPrepGroups <= kgroups && (reinterpret_cast<uintptr_t>(s) & 15) == 0;
+  if (whole) {
+    const uint4 lo = __ldg(reinterpret_cast<const uint4*>(src));
+    const uint4 hi = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int32_t kb = kb0 + j;
-      const uint32_t byte =
-          (r < rows && kb < kblocks) ? s[static_cast<int64_t>(r) * kblocks + kb] : 127u;
-      word |= byte << (8 * j);
-    }
+    for (int j = 0; j < kPrepGroups; ++j) dst[j * 128] = w[j];
+  } else {
+    for (int j = 0; j < kPrepGroups && g0 + j < kgroups; ++j)
+      dst[j * 128] = scale_word(s, r, rows, kblocks, g0 + j);
   }
-  out[(static_cast<int64_t>(rb) * kgroups + g) * 128 + t] = word;
 }
 
 cudaError_t mx_scale_prep(const uint8_t* a_scales, int64_t a_rows, int64_t a_row_blocks,
                           const uint8_t* b_scales, int64_t b_rows, int64_t b_row_blocks,
                           int64_t kblocks, int64_t kgroups, uint8_t* out, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>(kgroups), static_cast<unsigned>(a_row_blocks + b_row_blocks));
+  const dim3 grid(static_cast<unsigned>((kgroups + kPrepGroups - 1) / kPrepGroups),
+                  static_cast<unsigned>(a_row_blocks + b_row_blocks));
   mx_scale_prep_kernel<<<grid, 128, 0, stream>>>(
       a_scales, static_cast<int32_t>(a_rows), static_cast<int32_t>(a_row_blocks), b_scales,
       static_cast<int32_t>(b_rows), static_cast<int32_t>(kblocks), static_cast<int32_t>(kgroups),
