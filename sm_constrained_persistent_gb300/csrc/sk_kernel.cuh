@@ -79,6 +79,10 @@ struct Cfg {
   // its rows 64-127 from the next 8 KB of the ring (still inside shared memory), and those
   // accumulator rows lie at m >= M, which is never stored.
   static constexpr int kARows = kTall ? 64 : kBM;
+  // MMA rows: tall stages run M = 64 MMAs over exactly those rows (half the tensor-pipe time of
+  // M = 128 ones, which matters where few SMs stream B).  An M = 64 accumulator holds row r in
+  // tensor-memory lane 32 * (r / 16) + r % 16: the first 16 lanes of each warp's quarter.
+  static constexpr int kMmaM = kTall ? 64 : kBM;
   // MN-major tiles are blocks of 128 bytes (kAtom elements) x kTileK k-rows, kBoxBytes each;
   // one MMA's K advances kMnAdvance bytes through a block.
   static constexpr int kAtom = kF8 ? 128 : 64;
@@ -118,7 +122,7 @@ struct Cfg {
       kMx ? ((1u << 7) | (1u << 10) | (1u << 23) | (uint32_t(kBN >> 3) << 17) |
              (uint32_t(kBM >> 4) << 24))
           : ((1u << 4) | (kF8 ? 0u : ((1u << 7) | (1u << 10))) | (kAT ? (1u << 15) : 0u) |
-             (kBT ? 0u : (1u << 16)) | (uint32_t(kBN >> 3) << 17) | (uint32_t(kBM >> 4) << 24));
+             (kBT ? 0u : (1u << 16)) | (uint32_t(kBN >> 3) << 17) | (uint32_t(kMmaM >> 4) << 24));
   // (A/B format fields: bf16 = 1 for kind::f16, E4M3 = 0 for kind::f8f6f4)
 };
 
@@ -707,7 +711,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t tm, tn;
       tile_coords(plan, u.tile, tm, tn);
       const int64_t y_warp = static_cast<int64_t>(tm) * kBM + quarter * 32;
-      const int64_t m = y_warp + lane;
+      // (tall stages: this lane's accumulator row, or past the matrix for lanes 16-31)
+      const int64_t m = Cf::kMmaM == 64
+                            ? (lane < 16 ? static_cast<int64_t>(tm) * kBM + quarter * 16 + lane : args.M)
+                            : y_warp + lane;
       const int64_t n_tile = static_cast<int64_t>(tn) * kBN;
       bool has_next;
       {
@@ -839,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (n_rem > 1) load_partial8(pq, rem + 8 * kBM + kSlot4, kBM);
             }
           }
-          if (args.c_tma) {
+          if (args.c_tma && Cf::kMmaM == kBM) {   // (M = 64 accumulators: direct stores)
             store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_tile + ch * 32, y_warp, v);
           } else {
             store_row_chunk(args, m, n_tile + ch * 32, v);
