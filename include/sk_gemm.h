@@ -18,7 +18,12 @@
  *                       holding k = 0) acquires the flags, adds the partials, and only then
  *                       adds the bias along N and stores (tritonBLAS PR #67 "Fix StreamK Kernel
  *                       Bias", Motivation and Technical Details; tritonBLAS PR #74 "Stream-k
- *                       mxfp4 kernel": one P slot and one lock per CTA).
+ *                       mxfp4 kernel": one P slot and one lock per CTA).  In the bf16 and
+ *                       fp8 SM-pair kernels, where at least two CTAs have nothing to do but
+ *                       their piece of a tile the owner ends on, they and the owner each
+ *                       finish a share of its columns (the owner spills the others' share to
+ *                       a second slot); every element still gets each partial and the bias
+ *                       once.
  *   SK_MODE_HYBRID      the last (tiles mod g) tiles run Stream-K over all g CTAs (each CTA does
  *                       its Stream-K share first), the other tiles run whole, round-robin.
  *   SK_MODE_AUTO        the library picks the schedule (persistent, Stream-K or hybrid) and the

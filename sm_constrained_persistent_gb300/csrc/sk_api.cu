@@ -571,12 +571,14 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   if (opt != nullptr && opt->sm_record != nullptr && ctas > opt->sm_record_len)
     return SK_ERR_INVALID_ARG;
 
-  const size_t P_bytes = streamk ? static_cast<size_t>(ctas) * kTileM * plan.tile_n * sizeof(float) : 0;
+  // Flags and partial slots are needed only where tiles are split: one per CTA, and in the bf16
+  // and fp8 pairs a second one, for an owner's share of a tile that several CTAs finish.
+  const size_t slots = streamk ? static_cast<size_t>(ctas) * (pair && format != 1 ? 2 : 1) : 0;
+  const size_t P_bytes = slots * kTileM * plan.tile_n * sizeof(float);
   const MxLayout mx = mx_layout(plan);
   Workspace* ws = nullptr;
-  // Flags are needed only where tiles are split (one per CTA); whole-tile grids use none.
-  if ((st = ensure_workspace(dev, stream, P_bytes, streamk ? static_cast<size_t>(ctas) : 0,
-                             format == 1 ? mx.bytes() : 0, &ws)) != SK_OK)
+  if ((st = ensure_workspace(dev, stream, P_bytes, slots, format == 1 ? mx.bytes() : 0, &ws)) !=
+      SK_OK)
     return st;
   if (++ws->epoch == 0) ws->epoch = 1;
 
@@ -830,9 +832,10 @@ sk_status_t sk_workspace_reserve(int device, void* stream_ptr, int max_grid, int
     }
     Workspace* ws = nullptr;
     if (st == SK_OK)
+      // two slots and flags per CTA: the most any grid uses (bf16 and fp8 SM pairs)
       st = ensure_workspace(device, static_cast<cudaStream_t>(stream_ptr),
-                            static_cast<size_t>(max_grid) * kTileM * 256 * sizeof(float),
-                            static_cast<size_t>(max_grid), sf_bytes, &ws);
+                            2 * static_cast<size_t>(max_grid) * kTileM * 256 * sizeof(float),
+                            2 * static_cast<size_t>(max_grid), sf_bytes, &ws);
   }
   cudaSetDevice(prev);
   return st;

@@ -181,20 +181,23 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch,
 
 // Thread 0 of an owner's epilogue while its piece's k-loop may still run: waits for the flag of
 // one contributor, unless the k-loop finishes first (the accumulator's full barrier `full`
-// completes phase `parity`) or the CTA is aborting.  kPollFlag: the flag was seen and consumed,
-// so the partial can be summed into the idle accumulator now.  kPollLoopDone: the partial is
-// left to the drain, which reads it while it stores C.  kPollTimeout: no flag within the limit.
+// completes phase `parity`) or the CTA is aborting.  kPollFlag: the flag was seen (and, with
+// `consume`, cleared), so the partial can be summed into the idle accumulator now.
+// kPollLoopDone: the partial is left to the drain, which reads it while it stores C.
+// kPollTimeout: no flag within the limit.  (A flag holds the launch's epoch, so one left set
+// is never mistaken for a later launch's; clearing it is optional.  The pair kernels, whose
+// flags several CTAs may read, leave them set.)
 enum : uint32_t { kPollFlag = 0, kPollLoopDone = 1, kPollTimeout = 2 };
 __device__ __forceinline__ uint32_t poll_flag_or_full(uint32_t* flag, uint32_t epoch, uint64_t* full,
                                                       uint32_t parity,
                                                       volatile uint32_t* abort_flag,
-                                                      uint64_t timeout_ns) {
+                                                      uint64_t timeout_ns, bool consume = true) {
   const uint64_t t0 = global_timer_ns();
   uint32_t ns = 32;
   while (true) {
     if (mbar_test_wait(full, parity) || *abort_flag) return kPollLoopDone;
     if (flag_acquire(flag) == epoch) {
-      *reinterpret_cast<volatile uint32_t*>(flag) = 0u;   // consumed: ready for the next launch
+      if (consume) *reinterpret_cast<volatile uint32_t*>(flag) = 0u;
       return kPollFlag;
     }
     if (global_timer_ns() - t0 > timeout_ns) return kPollTimeout;
@@ -329,10 +332,12 @@ __device__ __forceinline__ bool tma_store_piece(const Args& a, const CUtensorMap
 // Adds the bias to columns [n0, n0+32) of this warp's 32 rows (rows y .. y+31, one per lane),
 // casts, and stores them through the warp's two 2 KB staging buffers (`stage`, alternating by
 // `buf`): one bf16 piece of 32 columns, or two fp32 pieces of 16.
+// (kAddBias = false: the caller has added the bias.)
+template <bool kAddBias = true>
 __device__ __forceinline__ void store_chunk_tma(const Args& a, const CUtensorMap* tmC,
                                                 uint8_t* stage, int& buf, int lane, int64_t n0,
                                                 int64_t y, float (&v)[32]) {
-  add_bias_chunk(a, n0, v);
+  if constexpr (kAddBias) add_bias_chunk(a, n0, v);
   if (a.out_bf16) {
     uint4 q[4];
 #pragma unroll
@@ -359,10 +364,11 @@ __device__ __forceinline__ void store_chunk_tma(const Args& a, const CUtensorMap
 // room for no more): pieces of 32 bytes of each of the warp's 32 rows -- 16 bf16 or 8 fp32
 // columns, two or four per 32-column chunk -- each stored by TMA (C's tensor map then has
 // 32 x 32-byte boxes, no swizzle) once the previous piece has been read out of the buffer.
+template <bool kAddBias = true>
 __device__ __forceinline__ void store_chunk_tma_1k(const Args& a, const CUtensorMap* tmC,
                                                    uint8_t* buf, int lane, int64_t n0, int64_t y,
                                                    float (&v)[32]) {
-  add_bias_chunk(a, n0, v);
+  if constexpr (kAddBias) add_bias_chunk(a, n0, v);
   const int cols = a.out_bf16 ? 16 : 8;   // columns per 32-byte piece
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
@@ -398,13 +404,15 @@ __device__ __forceinline__ void store_chunk_tma_1k(const Args& a, const CUtensor
   }
 }
 
-// Adds the bias, casts and stores 32 consecutive columns [n0, n0+32) of row m.
+// Adds the bias (unless kAddBias is false), casts and stores 32 consecutive columns [n0, n0+32)
+// of row m.
+template <bool kAddBias = true>
 __device__ __forceinline__ void store_row_chunk(const Args& a, int64_t m, int64_t n0,
                                                 float (&v)[32]) {
   if (m >= a.M) return;
   const bool full_chunk = (n0 + 32 <= a.N) && ((a.N & 7) == 0);
   if (a.out_bf16) {
-    const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(a.bias);
+    const __nv_bfloat16* bias = kAddBias ? static_cast<const __nv_bfloat16*>(a.bias) : nullptr;
     __nv_bfloat16* c = static_cast<__nv_bfloat16*>(a.C) + m * a.N + n0;
     if (full_chunk) {
       if (bias != nullptr) {
@@ -441,7 +449,7 @@ __device__ __forceinline__ void store_row_chunk(const Args& a, int64_t m, int64_
       }
     }
   } else {
-    const float* bias = static_cast<const float*>(a.bias);
+    const float* bias = kAddBias ? static_cast<const float*>(a.bias) : nullptr;
     float* c = static_cast<float*>(a.C) + m * a.N + n0;
     if (full_chunk) {
       if (bias != nullptr) {

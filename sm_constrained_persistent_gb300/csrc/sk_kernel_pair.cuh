@@ -23,6 +23,15 @@
 // MXFP4 keeps one accumulator (256 columns) so that the per-stage scale-factor slots fit in
 // the 512 tensor-memory columns; the fast drain keeps the MMA's wait for it short.  bf16 keeps
 // two accumulators.
+//
+// Shared finish (bf16, fp8): where a split tile's owner ends its range on that tile and at
+// least two of its contributors hold nothing but their piece of it, the owner and those
+// contributors each finish a share of the tile's 32-column chunks.  Each writes the other
+// parties' chunks of its accumulator to scratch (the owner to a second slot) and releases a
+// flag, then waits for the others' flags and adds their partials, the bias, and stores its
+// own chunks.  Every element still gets every partial and the bias exactly once.  Without it
+// the owner alone reads all the partials after its k-loop, while the contributors, done at
+// the same moment, sit idle: 1.5x faster Stream-K on 512 x 512 x 16384, 1.1x on 1024^2 x 16384.
 #pragma once
 
 #include "sk_kernel.cuh"
@@ -38,6 +47,33 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
+}
+
+// The bias of this lane's column in each of the four 32-column chunks of a warp's 128 columns
+// from n_half (0 past N), read when a piece starts so that no chunk's drain waits for it.
+__device__ __forceinline__ void load_bias_lanes(const Args& a, int64_t n_half, int lane,
+                                                float (&b)[4]) {
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    const int64_t n = n_half + ch * 32 + lane;
+    b[ch] = 0.0f;
+    if (a.bias != nullptr && n < a.N)
+      b[ch] = a.out_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.bias)[n])
+                         : static_cast<const float*>(a.bias)[n];
+  }
+}
+
+// b[i] for a loop index i, without indexing the array in local memory.
+__device__ __forceinline__ float pick4(const float (&b)[4], int i) {
+  return i == 0 ? b[0] : i == 1 ? b[1] : i == 2 ? b[2] : b[3];
+}
+
+// v[j] += the bias of column j of the chunk, held by lane j.  (Nothing is added without a
+// bias, so that a zero keeps its sign as in the other kernels.)
+__device__ __forceinline__ void add_bias_lanes(const Args& a, float (&v)[32], float b) {
+  if (a.bias == nullptr) return;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xffffffffu, b, j);
 }
 
 // Address of the same shared-memory location in cluster CTA `rank`.
@@ -191,6 +227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
   using Cf = PairCfg<kMx, kAT, kBT, kF8>;
   constexpr int S = Cf::kStages;
   constexpr int kBN = Cf::kBN;
+  constexpr bool kShare = Cf::kAccBufs == 2;   // shared tiles may be finished by several CTAs
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -462,20 +499,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
       const int64_t y_warp = static_cast<int64_t>(tm) * 256 + rank * 128 + quarter * 32;
       const int64_t m = y_warp + lane;
       const int64_t n_half = static_cast<int64_t>(tn) * kBN + half * 128;
+      float bias_l[4];   // read here, or after the staging below (whose registers it would take)
       bool has_next;
       {
         Cursor peek = cur;
         Unit later;
         has_next = peek.next(plan, later);
       }
+      // The tile's contributors, and which CTAs finish its columns.  Columns go in 32-column
+      // chunks, chunk j = 4 * half + ch to party j % parties; the owner is party 0.  Mostly the
+      // owner finishes the whole tile (parties = 1).  In the bf16 and fp8 pairs, when the
+      // owner's shared tile is its last piece and at least two contributors hold nothing else
+      // (finishers: contributor i is party i + 1), the finishers finish a share of the chunks
+      // each: they reach the end of their ranges with the owner, and sharing the tile spreads the
+      // partials' reads and the stores of C over all of them instead of queueing them on the
+      // owner.  With one finisher the owner keeps the tile: handing out half of it costs the
+      // owner about what the drain it saves does.
       int n_contrib = 0;
+      int parties = 1;
+      int party = 0;
+      int64_t owner = pair;
       if (u.role == kRoleOwner) {
-        int64_t covered = u.k1;
-        for (int64_t c = pair + 1; covered < plan.iters; ++c, ++n_contrib) {
-          const int64_t len = sk_range_len(plan, c);
-          covered += (len < plan.iters - covered) ? len : (plan.iters - covered);
+        const TileShare s = tile_contributors(plan, pair, u.k1);
+        n_contrib = s.n_contrib;
+        if (kShare && pair >= plan.whole_tiles && s.finishers >= 2) parties = 1 + s.finishers;
+      } else if (kShare && u.role == kRoleContrib) {
+        const int64_t first = (u.tile - plan.whole_tiles) * plan.iters;   // the tile's k = 0
+        const int64_t o = sk_range_cta(plan, first);
+        if (sk_range_begin(plan, pair) + sk_range_len(plan, pair) <= first + plan.iters &&
+            o >= plan.whole_tiles) {
+          const TileShare s =
+              tile_contributors(plan, o, sk_range_begin(plan, o) + sk_range_len(plan, o) - first);
+          if (s.finishers >= 2) {
+            owner = o;
+            n_contrib = s.n_contrib;
+            parties = 1 + s.finishers;
+            party = static_cast<int>(pair - o);
+          }
         }
       }
+      const bool shared_finish = parties > 1;
       // The shared tile an owner finishes with: no later piece waits for its accumulator, so it
       // is drained from tensor memory 32 columns at a time with the partials added (below).
       // With two accumulators, partials that are complete while its k-loop still runs are
@@ -483,6 +546,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
       // later piece uses it), so the fix-up after the loop reads tensor memory.
       const bool last_shared = u.role == kRoleOwner && !has_next && n_contrib > 0;
       const bool staged = Cf::kAccBufs == 2 && last_shared;
+      if (!staged) load_bias_lanes(args, n_half, lane, bias_l);
       uint32_t flag_status = kUnitStore;
       int n_staged = 0;   // contributors summed into the idle accumulator (the farthest ones)
       if (staged) {
@@ -498,7 +562,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
           if (et == 0) {
             const uint32_t r =
                 poll_flag_or_full(args.flags + 2 * (pair + 1 + c) + rank, args.epoch, &tfull[acc],
-                                  acc_phase, abort_flag, args.timeout_ns);
+                                  acc_phase, abort_flag, args.timeout_ns, false);
             if (r == kPollTimeout) record_error(args, kSiteFlag, u.tile);
             staged_status[i & 1] = r;
           }
@@ -515,21 +579,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
           n_staged = i + 1;
         }
       }
+      if (staged) load_bias_lanes(args, n_half, lane, bias_l);
       // contributors 0 .. n_rem-1 (the nearest) are read by the drain
       const int n_rem = flag_status == kUnitStore ? n_contrib - n_staged : 0;
       if (et == 0) {
         uint32_t status = kUnitStore;
         if (!wait_bar(&tfull[acc], acc_phase, abort_flag, args, kSiteEpilogue)) {
           status = kUnitAbort;
-        } else if (u.role == kRoleOwner) {
+        } else if (u.role == kRoleOwner && !shared_finish) {
+          // (Flags stay set: a finisher may read the same ones.)
           for (int c = 0; c < n_rem; ++c) {
-            uint32_t* f = args.flags + 2 * (pair + 1 + c) + rank;
-            if (!wait_flag(f, args.epoch, args.timeout_ns)) {
+            if (!wait_flag(args.flags + 2 * (pair + 1 + c) + rank, args.epoch, args.timeout_ns)) {
               record_error(args, kSiteFlag, u.tile);
               status = kUnitSkip;
               break;
             }
-            *reinterpret_cast<volatile uint32_t*>(f) = 0u;
           }
         }
         unit_status[parity] = status;
@@ -540,6 +604,123 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc) * Cf::kAccCols + half * 128;
+
+      if (shared_finish) {
+        // 1. Hand out: the owner writes the other parties' chunks of its own accumulator (not
+        //    the partials staged beside it) to its second slot, 2 * grid + cta; a finisher
+        //    writes every chunk but its own to its slot, as any contributor does.  Then the flag.
+        const bool is_owner = u.role == kRoleOwner;
+        const int64_t out_slot = is_owner ? 2 * static_cast<int64_t>(plan.grid) + cta : cta;
+        {
+          float4* out = reinterpret_cast<float4*>(args.P + out_slot * (kBM * kBN)) +
+                        static_cast<int64_t>(half * 4) * 8 * kBM + row;
+          const uint64_t policy = l2_policy_evict_last();
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
+            if ((4 * half + ch) % parties == party) continue;
+            uint32_t r[32];
+            __syncwarp();
+            tmem_load_32cols(t_row + ch * 32, r);
+            tmem_load_wait();
+            float4* dst = out + static_cast<int64_t>(ch) * 8 * kBM;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              st_cg_policy(dst + q * kBM,
+                           make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                       __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])),
+                           policy);
+          }
+        }
+        // 2. Wait for the other parties' partials of this CTA's chunks: for the owner, the
+        //    contributors not staged; for a finisher, the owner's second slot and every other
+        //    contributor.  (unit_status[parity ^ 1] is free: every thread read it before the
+        //    barrier above, and no piece follows this one.)
+        // (With more than 8 parties, those past the eighth finish no chunk and wait for nothing.)
+        const int n_src = party >= kBN / 32 ? 0 : (is_owner ? n_rem : n_contrib);
+        auto src_slot = [&](int s) -> int64_t {
+          if (is_owner) return 2 * (pair + 1 + s) + rank;
+          if (s == 0) return 2 * static_cast<int64_t>(plan.grid) + 2 * owner + rank;
+          const int c = (s - 1 < party - 1) ? s - 1 : s;   // contributors other than this one
+          return 2 * (owner + 1 + c) + rank;
+        };
+        __threadfence();
+        named_barrier_sync(1, kPairEpilogueThreads);
+        if (et == 0) {
+          if (!(args.inject_drop && cta == args.drop_cta))
+            flag_release(args.flags + out_slot, args.epoch);
+          uint32_t got = kUnitStore;
+          for (int s = 0; s < n_src; ++s) {
+            if (!wait_flag(args.flags + src_slot(s), args.epoch, args.timeout_ns)) {
+              record_error(args, kSiteFlag, u.tile);
+              got = kUnitSkip;
+              break;
+            }
+          }
+          unit_status[parity ^ 1] = got;
+        }
+        named_barrier_sync(1, kPairEpilogueThreads);
+        const bool store = unit_status[parity ^ 1] == kUnitStore && flag_status == kUnitStore;
+        // 3. Finish this CTA's chunks: its accumulator (+ the staged partials, owner) + the
+        //    partials read here + bias, cast and stored.
+        //    The first source of the next chunk is requested before this one is stored (one
+        //    more would not fit in the registers).
+        const uint32_t t_stage = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                 static_cast<uint32_t>(acc ^ 1) * Cf::kAccCols + half * 128;
+        auto mine = [&](int c) { return (4 * half + c) % parties == party; };
+        auto src = [&](int s, int c) {
+          return reinterpret_cast<const float4*>(args.P + src_slot(s) * (kBM * kBN)) +
+                 static_cast<int64_t>(half * 4 + c) * 8 * kBM + row;
+        };
+        int ch = 0;
+        while (ch < 4 && !mine(ch)) ++ch;
+        float4 pp[8];
+        if (store && ch < 4 && n_src > 0) load_partial8(pp, src(0, ch), kBM);
+#pragma unroll 1
+        while (ch < 4) {
+          int next = ch + 1;
+          while (next < 4 && !mine(next)) ++next;
+          uint32_t own[32];
+          float w[32];
+          __syncwarp();
+          tmem_load_32cols(t_row + ch * 32, own);
+          if (is_owner && n_staged > 0) {
+            uint32_t part[32];
+            tmem_load_32cols(t_stage + ch * 32, part);
+            tmem_load_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(own[j]) + __uint_as_float(part[j]);
+          } else {
+            tmem_load_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) w[j] = __uint_as_float(own[j]);
+          }
+          if (store) {
+            if (n_src > 0) add_partial8(w, pp, false);
+#pragma unroll 1
+            for (int s = 1; s < n_src; s += 2) {
+              float4 pq[8];
+              load_partial8(pp, src(s, ch), kBM);
+              if (s + 1 < n_src) load_partial8(pq, src(s + 1, ch), kBM);
+              add_partial8(w, pp, false);
+              if (s + 1 < n_src) add_partial8(w, pq, false);
+            }
+            if (next < 4 && n_src > 0) load_partial8(pp, src(0, next), kBM);
+            add_bias_lanes(args, w, pick4(bias_l, ch));
+            if constexpr (Cf::kTmaStore) {
+              store_chunk_tma<false>(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
+            } else if (args.c_tma) {
+              store_chunk_tma_1k<false>(args, &tmC, my_stage, lane, n_half + ch * 32, y_warp, w);
+            } else {
+              store_row_chunk<false>(args, m, n_half + ch * 32, w);
+            }
+          }
+          ch = next;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) remote_arrive(tempty_leader0 + acc * 8);
+        break;   // the last piece
+      }
 
       if (last_shared) {
         // Last piece: no later piece waits for this accumulator, so add and store it 32
@@ -593,12 +774,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
           if (store) {
             // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8);
             // MXFP4 ones when N allows
+            add_bias_lanes(args, w, pick4(bias_l, ch));
             if constexpr (Cf::kTmaStore) {
-              store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
+              store_chunk_tma<false>(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else if (args.c_tma) {
-              store_chunk_tma_1k(args, &tmC, my_stage, lane, n_half + ch * 32, y_warp, w);
+              store_chunk_tma_1k<false>(args, &tmC, my_stage, lane, n_half + ch * 32, y_warp, w);
             } else {
-              store_row_chunk(args, m, n_half + ch * 32, w);
+              store_row_chunk<false>(args, m, n_half + ch * 32, w);
             }
           }
         }
@@ -640,12 +822,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
             }
             // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8);
             // MXFP4 ones when N allows
+            add_bias_lanes(args, w, pick4(bias_l, ch));
             if constexpr (Cf::kTmaStore) {
-              store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
+              store_chunk_tma<false>(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else if (args.c_tma) {
-              store_chunk_tma_1k(args, &tmC, my_stage, lane, n_half + ch * 32, y_warp, w);
+              store_chunk_tma_1k<false>(args, &tmC, my_stage, lane, n_half + ch * 32, y_warp, w);
             } else {
-              store_row_chunk(args, m, n_half + ch * 32, w);
+              store_row_chunk<false>(args, m, n_half + ch * 32, w);
             }
           }
         }
@@ -707,12 +890,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
             float(&w)[32] = *reinterpret_cast<float(*)[32]>(&v[ch * 32]);
             // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8);
             // MXFP4 ones when N allows
+            add_bias_lanes(args, w, pick4(bias_l, ch));
             if constexpr (Cf::kTmaStore) {
-              store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
+              store_chunk_tma<false>(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else if (args.c_tma) {
-              store_chunk_tma_1k(args, &tmC, my_stage, lane, n_half + ch * 32, y_warp, w);
+              store_chunk_tma_1k<false>(args, &tmC, my_stage, lane, n_half + ch * 32, y_warp, w);
             } else {
-              store_row_chunk(args, m, n_half + ch * 32, w);
+              store_row_chunk<false>(args, m, n_half + ch * 32, w);
             }
           }
         }

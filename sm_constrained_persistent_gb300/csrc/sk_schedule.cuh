@@ -14,7 +14,8 @@
 // inside a tile, so a CTA spills at most once (one scratch slot per CTA, as in tritonBLAS PR
 // #74 "Stream-k mxfp4 kernel"), and the tile a CTA owns but shares is the one its range ends
 // in, continued by CTAs c+1, c+2, ...  The order in which a CTA runs its pieces is given by
-// Cursor below.
+// Cursor below.  (The SM-pair kernels may split the owner's fix-up of a tile among the owner
+// and contributors that have no other piece; see tile_contributors.)
 //
 // Linear tile index -> (tile row, tile column) goes through two bijections:
 //  1. In the Stream-K region, the tau-th tile owned by CTA c is given raster position
@@ -59,6 +60,37 @@ __host__ __device__ __forceinline__ int64_t sk_range_begin(const Plan& p, int64_
 
 __host__ __device__ __forceinline__ int64_t sk_range_len(const Plan& p, int64_t cta) {
   return p.sk_base + (cta < p.sk_extra ? 1 : 0);
+}
+
+// The CTA whose range holds Stream-K region iteration x.
+__host__ __device__ __forceinline__ int64_t sk_range_cta(const Plan& p, int64_t x) {
+  const int64_t long_span = p.sk_extra * (p.sk_base + 1);  // iterations of the longer ranges
+  if (x < long_span) return x / (p.sk_base + 1);
+  return p.sk_base > 0 ? p.sk_extra + (x - long_span) / p.sk_base : p.sk_extra;
+}
+
+// The CTAs that continue the shared tile CTA `owner` owns, whose own piece is the tile's first
+// `owned` k-iterations: CTAs owner+1, owner+2, ..., `n_contrib` of them.  The first
+// `finishers` of them hold nothing but their piece of this tile: their ranges begin inside it
+// and end inside it or at its end.  (Every contributor but the last lies inside the tile; the
+// last one is a finisher when its range ends at the tile's end.)
+struct TileShare {
+  int32_t n_contrib;
+  int32_t finishers;
+};
+
+__host__ __device__ __forceinline__ TileShare tile_contributors(const Plan& p, int64_t owner,
+                                                                int64_t owned) {
+  TileShare s = {0, 0};
+  int64_t covered = owned;
+  for (int64_t c = owner + 1; covered < p.iters; ++c) {
+    const int64_t len = sk_range_len(p, c);
+    const int64_t room = p.iters - covered;
+    if (len <= room) ++s.finishers;
+    covered += len < room ? len : room;
+    ++s.n_contrib;
+  }
+  return s;
 }
 
 // Walks one CTA's pieces in execution order:
@@ -151,14 +183,7 @@ __host__ __device__ __forceinline__ int32_t unit_k(const Unit& u, int32_t i) {
 __host__ __device__ __forceinline__ int64_t raster_position(const Plan& p, int64_t t) {
   if (t < p.whole_tiles) return t;
   const int64_t local = t - p.whole_tiles;
-  const int64_t x = local * p.iters;                       // its k = 0 iteration
-  const int64_t long_span = p.sk_extra * (p.sk_base + 1);  // iterations of the longer ranges
-  int64_t c;                                               // owner: the CTA whose range holds x
-  if (x < long_span) {
-    c = x / (p.sk_base + 1);
-  } else {
-    c = p.sk_base > 0 ? p.sk_extra + (x - long_span) / p.sk_base : p.sk_extra;
-  }
+  const int64_t c = sk_range_cta(p, local * p.iters);      // owner: holds the tile's k = 0
   const int64_t start = sk_range_begin(p, c);
   const int64_t first_owned = (start + p.iters - 1) / p.iters;   // first tile whose k = 0 is c's
   const int64_t tau = local - first_owned;

@@ -381,9 +381,82 @@ def test_streamk_fixup_with_many_and_late_contributors_is_bit_exact(mode, shape,
     want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]),
                                oracle.BF16 if out == "bf16" else oracle.F32)
     want_bits = want if out == "bf16" else want.view(np.uint32)
-    for _ in range(2):   # the second launch reuses flags the first one's owners cleared
+    for _ in range(2):   # the second launch finds the first one's flags (cleared or left set)
         c = gu.run_bf16(p, out=out, mode=mode, num_sms=num_sms, options=TILES[tile])
         assert np.array_equal(gu.host_bits(c), want_bits)
+
+
+# ---- split pair tiles finished by several pairs ---------------------------------------------
+
+def finishing_parties(plan):
+    """{tile: number of pairs that finish its columns} for the split tiles of a Stream-K plan
+    without whole tiles: the owner plus each contributor whose only piece is its piece of the
+    tile, when there are at least two such contributors; else the owner alone."""
+    segs = sk.sk_plan_segments(plan)
+    pieces = np.bincount(segs[:, 0], minlength=plan.grid)
+    out = {}
+    for tile in np.unique(segs[segs[:, 4] == 1, 1]):
+        contrib = segs[(segs[:, 1] == tile) & (segs[:, 4] == 2), 0]
+        finishers = int((pieces[contrib] == 1).sum())
+        out[int(tile)] = 1 + finishers if finishers >= 2 else 1
+    return out
+
+
+@pytest.mark.parametrize("shape,num_sms,parties", [
+    ((300, 264, 8200), 16, {1, 3}),        # ragged M, N and K
+    ((300, 264, 8200), 40, {4, 5, 6}),
+    ((300, 264, 8200), 64, {7, 8, 9}),     # more parties than the tile's eight column chunks
+    ((520, 776, 4096), 152, {5, 6, 7}),
+    ((256, 256, 16384), 152, {76}),        # one tile, every pair on it
+])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_tiles_finished_by_several_pairs_are_bit_exact(shape, num_sms, parties, out):
+    M, N, K = shape
+    plan = sk.sk_plan(0, M, N, K, num_sms, "streamk", torch.cuda.get_device_properties(0).multi_processor_count,
+                      TILES["pair256"])
+    assert plan.ctas_per_tile == 2 and set(finishing_parties(plan).values()) == parties
+    p = inputs.bf16_problem(M, N, K, seed=M + N + K + num_sms, integer=True,
+                            bias="bf16_int" if out == "bf16" else "f32_int")
+    want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]),
+                               oracle.BF16 if out == "bf16" else oracle.F32)
+    want_bits = want if out == "bf16" else want.view(np.uint32)
+    for _ in range(2):
+        c = gu.run_bf16(p, out=out, mode="streamk", num_sms=num_sms, options=TILES["pair256"])
+        assert np.array_equal(gu.host_bits(c), want_bits)
+
+
+def test_tiles_finished_by_several_pairs_random_inputs_match_oracle():
+    p = inputs.bf16_problem(512, 512, 8192, seed=31, operand_scale="sqrt_k", bias="bf16_uniform")
+    c = gu.run_bf16(p, out="bf16", mode="streamk", num_sms=38, options=TILES["pair256"])
+    ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "bf16")
+    gu.assert_close(gu.host_values(c), ref, "bf16")
+
+
+@pytest.mark.parametrize("dropped", ["finisher", "owner"])
+def test_shared_finish_wait_that_runs_out_reports_timeout(dropped):
+    # 512 x 512 x 4096 on 10 pairs: two split tiles are finished by their owner and two
+    # finishers.  A dropped finisher leaves the owner and the other finisher waiting for its
+    # partial; a dropped owner leaves the finishers waiting for the owner's share.
+    M, N, K = 512, 512, 4096
+    opts = dict(TILES["pair256"])
+    plan = sk.sk_plan(0, M, N, K, 20, "streamk", torch.cuda.get_device_properties(0).multi_processor_count, opts)
+    parties = finishing_parties(plan)
+    assert set(parties.values()) == {1, 3}
+    segs = sk.sk_plan_segments(plan)
+    tile = min(t for t, n in parties.items() if n == 3)
+    owner = int(segs[(segs[:, 1] == tile) & (segs[:, 4] == 1), 0][0])
+    drop_pair = owner if dropped == "owner" else owner + 1
+    p = inputs.bf16_problem(M, N, K, seed=9, integer=True, bias="bf16_int")
+    a, b, bias = gu.dev_bf16(p["A"]), gu.dev_bf16(p["B"]), gu.dev_bias(p["bias"])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        sk.gemm_bf16(a, b, bias, mode="streamk", num_sms=20, stream=s,
+                     options={**opts, "inject_faults": 1, "drop_release_cta": 2 * drop_pair,
+                              "spin_timeout_ns": 20_000_000})
+    assert sk.sk_stream_status(s.cuda_stream) == sk.SK_ERR_TIMEOUT
+    c = gu.run_bf16(p, out="bf16", mode="streamk", num_sms=20, stream=s, options=opts)
+    want = oracle.round_output(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), oracle.BF16)
+    assert np.array_equal(gu.host_bits(c), want)
 
 
 # ---- 96-wide tiles (one row of tiles streaming B over more SMs) -----------------------------

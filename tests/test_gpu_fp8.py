@@ -48,6 +48,20 @@ def test_integer_inputs_are_bit_exact(mode, shape, out, tile):
     assert np.array_equal(gu.host_bits(c), _want_bits(p, out))
 
 
+@pytest.mark.parametrize("shape,num_sms", [((300, 272, 16400), 16), ((300, 272, 16400), 64),
+                                           ((520, 784, 8192), 152), ((512, 512, 16384), 152)])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_split_pair_tiles_finished_by_several_pairs_are_bit_exact(shape, num_sms, out):
+    # where at least two pairs have their whole Stream-K range in one tile, they finish a share
+    # of its columns with the tile's owner (3 to 22 pairs per tile here)
+    M, N, K = shape
+    p = inputs.fp8_problem(M, N, K, seed=M + N + K, integer=True,
+                           bias="f32_int" if out == "f32" else "none")
+    for _ in range(2):
+        c = run_fp8(p, out=out, mode="streamk", num_sms=num_sms, options=TILES["pair256"])
+        assert np.array_equal(gu.host_bits(c), _want_bits(p, out))
+
+
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("num_sms", [1, 3, 17, 0])
 @pytest.mark.parametrize("tile", ["auto", "128x128", "pair256"])
