@@ -23,7 +23,8 @@
  *                       their piece of a tile the owner ends on, they and the owner each
  *                       finish a share of its columns (the owner spills the others' share to
  *                       a second slot); every element still gets each partial and the bias
- *                       once.
+ *                       once.  (Not in calls captured into a CUDA graph, whose replays share
+ *                       one flag epoch: there the owner finishes every tile.)
  *   SK_MODE_HYBRID      the last (tiles mod g) tiles run Stream-K over all g CTAs (each CTA does
  *                       its Stream-K share first), the other tiles run whole, round-robin.
  *   SK_MODE_AUTO        the library picks the schedule (persistent, Stream-K or hybrid) and the

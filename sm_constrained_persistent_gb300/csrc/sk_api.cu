@@ -651,6 +651,11 @@ sk_status_t run_gemm(int format, const void* A, const void* A_scale, const void*
   a.flags = ws->flags;
   a.err = ws->err;
   a.c_tma = c_tma ? 1 : 0;
+  if (streamk) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return SK_ERR_CUDA;
+    a.replay = cs != cudaStreamCaptureStatusNone ? 1 : 0;
+  }
   a.sm_record = opt != nullptr ? static_cast<uint32_t*>(opt->sm_record) : nullptr;
   a.timeout_ns = static_cast<uint64_t>(
       opt != nullptr && opt->spin_timeout_ns > 0 ? opt->spin_timeout_ns : kDefaultTimeoutNs);

@@ -24,7 +24,8 @@ struct Args {
   const uint8_t* sfb;
   int64_t sf_kgroups;    // k groups (4 scale blocks = 128 K elements each) per row block
   int32_t c_tma;         // one-CTA kernels: 1 = C is written through the tmC tensor map
-  int32_t pad_;
+  int32_t replay;        // 1: the launch is captured into a CUDA graph, so every replay sees the
+                         // same epoch; each flag is then cleared by its one reader
   uint32_t* sm_record;   // null, or one entry per CTA: the SM it ran on
 };
 

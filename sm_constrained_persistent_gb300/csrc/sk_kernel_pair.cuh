@@ -32,6 +32,9 @@
 // own chunks.  Every element still gets every partial and the bias exactly once.  Without it
 // the owner alone reads all the partials after its k-loop, while the contributors, done at
 // the same moment, sit idle: 1.5x faster Stream-K on 512 x 512 x 16384, 1.1x on 1024^2 x 16384.
+// A flag may then have several readers, so flags are not cleared once read: each launch
+// releases them with a new epoch.  A launch captured into a CUDA graph keeps one epoch for all
+// its replays; it finishes every tile by its owner alone, which clears each flag it reads.
 #pragma once
 
 #include "sk_kernel.cuh"
@@ -522,8 +525,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
       if (u.role == kRoleOwner) {
         const TileShare s = tile_contributors(plan, pair, u.k1);
         n_contrib = s.n_contrib;
-        if (kShare && pair >= plan.whole_tiles && s.finishers >= 2) parties = 1 + s.finishers;
-      } else if (kShare && u.role == kRoleContrib) {
+        if (kShare && !args.replay && pair >= plan.whole_tiles && s.finishers >= 2)
+          parties = 1 + s.finishers;
+      } else if (kShare && !args.replay && u.role == kRoleContrib) {
         const int64_t first = (u.tile - plan.whole_tiles) * plan.iters;   // the tile's k = 0
         const int64_t o = sk_range_cta(plan, first);
         if (sk_range_begin(plan, pair) + sk_range_len(plan, pair) <= first + plan.iters &&
@@ -562,7 +566,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
           if (et == 0) {
             const uint32_t r =
                 poll_flag_or_full(args.flags + 2 * (pair + 1 + c) + rank, args.epoch, &tfull[acc],
-                                  acc_phase, abort_flag, args.timeout_ns, false);
+                                  acc_phase, abort_flag, args.timeout_ns, args.replay != 0);
             if (r == kPollTimeout) record_error(args, kSiteFlag, u.tile);
             staged_status[i & 1] = r;
           }
@@ -587,13 +591,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
         if (!wait_bar(&tfull[acc], acc_phase, abort_flag, args, kSiteEpilogue)) {
           status = kUnitAbort;
         } else if (u.role == kRoleOwner && !shared_finish) {
-          // (Flags stay set: a finisher may read the same ones.)
           for (int c = 0; c < n_rem; ++c) {
-            if (!wait_flag(args.flags + 2 * (pair + 1 + c) + rank, args.epoch, args.timeout_ns)) {
+            uint32_t* f = args.flags + 2 * (pair + 1 + c) + rank;
+            if (!wait_flag(f, args.epoch, args.timeout_ns)) {
               record_error(args, kSiteFlag, u.tile);
               status = kUnitSkip;
               break;
             }
+            // A captured launch keeps its epoch across replays, so its one reader clears the
+            // flag; otherwise every launch has a new epoch and the flag may stay set.
+            if (args.replay) *reinterpret_cast<volatile uint32_t*>(f) = 0u;
           }
         }
         unit_status[parity] = status;
@@ -637,12 +644,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
         //    barrier above, and no piece follows this one.)
         // (With more than 8 parties, those past the eighth finish no chunk and wait for nothing.)
         const int n_src = party >= kBN / 32 ? 0 : (is_owner ? n_rem : n_contrib);
-        auto src_slot = [&](int s) -> int64_t {
-          if (is_owner) return 2 * (pair + 1 + s) + rank;
-          if (s == 0) return 2 * static_cast<int64_t>(plan.grid) + 2 * owner + rank;
-          const int c = (s - 1 < party - 1) ? s - 1 : s;   // contributors other than this one
-          return 2 * (owner + 1 + c) + rank;
-        };
+        // Source s of this thread's row: s = 0 is `first` (the owner's second slot for a
+        // finisher, the nearest contributor for the owner); s >= 1 the next contributors, from
+        // `rest` on, one slot pair apart, skipping this CTA's own.
+        constexpr int64_t kSlot = kBM * kBN / 4;   // float4s per slot
+        const int64_t c0 = 2 * (owner + 1) + rank;  // slot of the tile's first contributor
+        const float4* first =
+            reinterpret_cast<const float4*>(args.P) + static_cast<int64_t>(half * 4) * 8 * kBM + row +
+            (is_owner ? c0 : 2 * static_cast<int64_t>(plan.grid) + 2 * owner + rank) * kSlot;
+        const float4* rest = reinterpret_cast<const float4*>(args.P) +
+                             static_cast<int64_t>(half * 4) * 8 * kBM + row +
+                             (is_owner ? c0 + 2 : c0) * kSlot;
+        const int skip = is_owner ? 1 << 30 : party - 1;
         __threadfence();
         named_barrier_sync(1, kPairEpilogueThreads);
         if (et == 0) {
@@ -650,7 +663,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
             flag_release(args.flags + out_slot, args.epoch);
           uint32_t got = kUnitStore;
           for (int s = 0; s < n_src; ++s) {
-            if (!wait_flag(args.flags + src_slot(s), args.epoch, args.timeout_ns)) {
+            const int64_t slot =
+                s == 0 ? (is_owner ? c0 : 2 * static_cast<int64_t>(plan.grid) + 2 * owner + rank)
+                       : (is_owner ? c0 + 2 * s : c0 + 2 * (s - 1 < skip ? s - 1 : s));
+            if (!wait_flag(args.flags + slot, args.epoch, args.timeout_ns)) {
               record_error(args, kSiteFlag, u.tile);
               got = kUnitSkip;
               break;
@@ -668,8 +684,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
                                  static_cast<uint32_t>(acc ^ 1) * Cf::kAccCols + half * 128;
         auto mine = [&](int c) { return (4 * half + c) % parties == party; };
         auto src = [&](int s, int c) {
-          return reinterpret_cast<const float4*>(args.P + src_slot(s) * (kBM * kBN)) +
-                 static_cast<int64_t>(half * 4 + c) * 8 * kBM + row;
+          const float4* b = s == 0 ? first : rest + (s - 1 < skip ? s - 1 : s) * 2 * kSlot;
+          return b + static_cast<int64_t>(c) * 8 * kBM;
         };
         int ch = 0;
         while (ch < 4 && !mine(ch)) ++ch;
