@@ -146,18 +146,30 @@ sk_status_t make_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, 
 // ---- automatic schedule and tile choice ---------------------------------------------------
 //
 // Estimated time of a plan, in microseconds.  The constants were fitted (least squares on the
-// relative error, non-negative) to the measured times of 32 bf16 shapes (from 64x14336x4096
-// to 8192^3, square, skinny, long-K and wave-boundary cases) under every schedule and tile
-// kind on a 152-SM GB300; on those shapes the cheapest estimate picks a configuration within
-// 1.2 % of the fastest on average, 11 % at most.
+// relative error, non-negative) to the measured times of 40 bf16 shapes (from 64x14336x4096
+// to 8192^3, square, skinny, long-K, few-tile and wave-boundary cases) under every schedule
+// and tile kind on a 152-SM GB300; on those shapes the cheapest estimate picks a
+// configuration within 0.6 % of the fastest on average, 4.3 % at most.
 struct CostModel {
   double t_iter[3];   // one k-iteration of a bf16 tile: SM pair 256x256x64, 128x256x64, 128x128x64
   double t_piece;     // each piece of work a CTA runs (tile hand-over, pipeline refill)
   double t_split;     // a Stream-K region whose tiles are split between CTAs (spill + fix-up)
   double t_part;      // each CTA that shares one split tile
   double t_launch;    // launch and first loads
+  double t_split_shared;   // t_split and t_part where SM pairs share the finish of their split
+  double t_part_shared;    // tiles (shared_finish below)
 };
-constexpr CostModel kCost = {{0.3048, 0.3358, 0.2516}, 0.7958, 5.3951, 2.2353, 10.8804};
+constexpr CostModel kCost = {{0.2836, 0.3321, 0.2501}, 1.021, 4.248, 2.0208, 10.6876,
+                             9.9955, 0.3779};
+
+// Whether the SM-pair kernels (bf16, fp8) finish most split tiles of a plan together with the
+// contributors that hold nothing else: a Stream-K region over the whole grid's work whose
+// ranges are at most a third of a tile, so that tiles have two such contributors or more.
+bool shared_finish(const sk_plan_t& p, int format) {
+  if (p.ctas_per_tile != 2 || format == 1 || p.sk_tiles == 0 || p.whole_tiles != 0) return false;
+  const int64_t per = ceil_div(p.sk_tiles * p.iters, std::max<int64_t>(p.grid, 1));
+  return ceil_div(static_cast<int64_t>(p.iters), std::max<int64_t>(per, 1)) >= 3;
+}
 // A k-iteration carries the same operand bytes in every format; an MXFP4 one (plus its scale
 // copies) takes ~1.45 times a bf16 one (8192^3 persistent: 0.44 vs 0.30 us), fp8 the same.
 constexpr double kMxIterScale = 1.45;
@@ -186,8 +198,10 @@ double plan_cost(const sk_plan_t& p, int format) {
     pieces = static_cast<double>(ceil_div(whole, g) + (skT > 0 ? ceil_div(per, I) + 1 : 0));
     if (skT > 0) {
       const bool split = per % I != 0 || (skT * I) % g != 0;
-      fixup = (split ? kCost.t_split : 0.0) +
-              kCost.t_part * static_cast<double>(ceil_div(I, std::max<int64_t>(per, 1)));
+      const bool shared = shared_finish(p, format);
+      fixup = (split ? (shared ? kCost.t_split_shared : kCost.t_split) : 0.0) +
+              (shared ? kCost.t_part_shared : kCost.t_part) *
+                  static_cast<double>(ceil_div(I, std::max<int64_t>(per, 1)));
     }
   }
   return kCost.t_launch + iters * t_iter + pieces * kCost.t_piece + fixup;
@@ -212,6 +226,8 @@ sk_status_t auto_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, 
     // GB300 than 256-column ones whatever the k-iteration count says: 64x14336x4096 31 vs
     // 38 us, 128x4096x11008 37 vs 55 us, 96x8192x8192 40 vs 49 us (best schedule of each).
     if (base.tile_n == 0 && M <= 128 && t.m == 128 && t.n == 256) continue;
+    // ... and no SM-pair tile, half of whose 256 rows would be empty.
+    if (base.tile_m == 0 && M <= 128 && t.m == 256) continue;
     // 96-wide tiles: one row of tiles, bf16 in the plain layout
     if (t.n == 96 && (format != 0 || layout != 0 || M > 128) && base.tile_n != 96) continue;
     for (int mode : modes) {

@@ -549,7 +549,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
       // summed into the idle one meanwhile (it held the previous piece, already drained; no
       // later piece uses it), so the fix-up after the loop reads tensor memory.
       const bool last_shared = u.role == kRoleOwner && !has_next && n_contrib > 0;
-      const bool staged = Cf::kAccBufs == 2 && last_shared;
+      // (An owner that shares its tile's finish does not stage: it needs only its own chunks of
+      // each partial, and its share, which the finishers wait for, goes out first.)
+      const bool staged = Cf::kAccBufs == 2 && last_shared && !shared_finish;
       if (!staged) load_bias_lanes(args, n_half, lane, bias_l);
       uint32_t flag_status = kUnitStore;
       int n_staged = 0;   // contributors summed into the idle accumulator (the farthest ones)
@@ -586,24 +588,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
       if (staged) load_bias_lanes(args, n_half, lane, bias_l);
       // contributors 0 .. n_rem-1 (the nearest) are read by the drain
       const int n_rem = flag_status == kUnitStore ? n_contrib - n_staged : 0;
-      if (et == 0) {
+      if (et < 32) {
+        // Lane 0 of the first epilogue warp waits for the accumulator; an owner finishing its
+        // tile alone then waits for its remaining contributors' flags, lane l for contributors
+        // l, l + 32, ... side by side.
         uint32_t status = kUnitStore;
-        if (!wait_bar(&tfull[acc], acc_phase, abort_flag, args, kSiteEpilogue)) {
+        if (et == 0 && !wait_bar(&tfull[acc], acc_phase, abort_flag, args, kSiteEpilogue))
           status = kUnitAbort;
-        } else if (u.role == kRoleOwner && !shared_finish) {
-          for (int c = 0; c < n_rem; ++c) {
+        status = __shfl_sync(0xffffffffu, status, 0);
+        if (status == kUnitStore && u.role == kRoleOwner && !shared_finish) {
+          bool ok = true;
+          for (int c = et; c < n_rem && ok; c += 32) {
             uint32_t* f = args.flags + 2 * (pair + 1 + c) + rank;
-            if (!wait_flag(f, args.epoch, args.timeout_ns)) {
-              record_error(args, kSiteFlag, u.tile);
-              status = kUnitSkip;
-              break;
-            }
+            ok = wait_flag(f, args.epoch, args.timeout_ns);
             // A captured launch keeps its epoch across replays, so its one reader clears the
             // flag; otherwise every launch has a new epoch and the flag may stay set.
-            if (args.replay) *reinterpret_cast<volatile uint32_t*>(f) = 0u;
+            if (ok && args.replay) *reinterpret_cast<volatile uint32_t*>(f) = 0u;
+          }
+          if (!__all_sync(0xffffffffu, ok)) {
+            if (et == 0) record_error(args, kSiteFlag, u.tile);
+            status = kUnitSkip;
           }
         }
-        unit_status[parity] = status;
+        if (et == 0) unit_status[parity] = status;
       }
       named_barrier_sync(1, kPairEpilogueThreads);
       const uint32_t status = unit_status[parity];
@@ -658,21 +665,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
         const int skip = is_owner ? 1 << 30 : party - 1;
         __threadfence();
         named_barrier_sync(1, kPairEpilogueThreads);
-        if (et == 0) {
-          if (!(args.inject_drop && cta == args.drop_cta))
+        if (et < 32) {
+          // The first epilogue warp: lane 0 releases this CTA's flag, then lane l waits for
+          // sources l, l + 32, ..., so the flags are polled side by side rather than one
+          // round trip to L2 after another.
+          if (et == 0 && !(args.inject_drop && cta == args.drop_cta))
             flag_release(args.flags + out_slot, args.epoch);
-          uint32_t got = kUnitStore;
-          for (int s = 0; s < n_src; ++s) {
+          bool ok = true;
+          for (int s = et; s < n_src && ok; s += 32) {
             const int64_t slot =
                 s == 0 ? (is_owner ? c0 : 2 * static_cast<int64_t>(plan.grid) + 2 * owner + rank)
                        : (is_owner ? c0 + 2 * s : c0 + 2 * (s - 1 < skip ? s - 1 : s));
-            if (!wait_flag(args.flags + slot, args.epoch, args.timeout_ns)) {
-              record_error(args, kSiteFlag, u.tile);
-              got = kUnitSkip;
-              break;
-            }
+            ok = wait_flag(args.flags + slot, args.epoch, args.timeout_ns);
           }
-          unit_status[parity ^ 1] = got;
+          ok = __all_sync(0xffffffffu, ok);
+          if (et == 0) {
+            if (!ok) record_error(args, kSiteFlag, u.tile);
+            unit_status[parity ^ 1] = ok ? kUnitStore : kUnitSkip;
+          }
         }
         named_barrier_sync(1, kPairEpilogueThreads);
         const bool store = unit_status[parity ^ 1] == kUnitStore && flag_status == kUnitStore;

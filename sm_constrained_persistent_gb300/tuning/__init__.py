@@ -69,7 +69,7 @@ def _features(M, N, K, tile, mode, sm_count):
     p = sk.sk_plan(0, M, N, K, 0, mode, sm_count, TILES[tile])
     g, T, I = p.grid, p.tiles, p.iters
     kind = ["pair", "128x256", "128x128"].index(tile)
-    x = [0.0] * 8
+    x = [0.0] * 10
     if mode in ("dp", "persistent"):
         workers = min(g, sm_count // p.ctas_per_tile)
         waves = math.ceil(T / workers)
@@ -80,16 +80,33 @@ def _features(M, N, K, tile, mode, sm_count):
         per = math.ceil(skT * I / g) if skT else 0
         x[kind] = per + math.ceil(whole / g) * I
         x[3] = math.ceil(whole / g) + (math.ceil(per / I) + 1 if skT else 0)
-        x[4] = 1.0 if skT and (per % I != 0 or (skT * I) % g != 0) else 0.0
-        x[5] = math.ceil(I / per) if skT else 0
+        split = 1.0 if skT and (per % I != 0 or (skT * I) % g != 0) else 0.0
+        sharers = math.ceil(I / per) if skT else 0
+        # SM pairs (bf16, fp8) finish a split tile together with the contributors that hold
+        # nothing else, where the tile has at least two of them: a fix-up of its own price
+        if shared_finish(p):
+            x[8], x[9] = split, sharers
+        else:
+            x[4], x[5] = split, sharers
     x[6] = 1.0
     return x
 
 
+def shared_finish(p, format=0):
+    """Whether a plan's split tiles are mostly finished by their owners and the contributors
+    that hold nothing else (the SM-pair kernels, bf16 and fp8): a Stream-K region covering the
+    whole grid's work, ranges at most a third of a tile."""
+    if p.ctas_per_tile != 2 or format == 1 or p.sk_tiles == 0 or p.whole_tiles != 0:
+        return False
+    per = math.ceil(p.sk_tiles * p.iters / max(p.grid, 1))
+    return math.ceil(p.iters / per) >= 3
+
+
 def fit(times, sm_count=152):
     """Constants (us): per-k-iteration time of a pair / 128x256 / 128x128 tile, per piece,
-    per split region, per CTA sharing a split tile, launch, and the data-parallel per-wave cost
-    (which only keeps data-parallel rows from biasing the others).  Also returns the mean and
+    per split region, per CTA sharing a split tile, launch, the data-parallel per-wave cost
+    (which only keeps data-parallel rows from biasing the others), and the split-region and
+    per-sharing-CTA costs where SM pairs share the finish of their split tiles.  Also returns the mean and
     the largest loss of picking the cheapest estimate among persistent / Stream-K / hybrid."""
     import numpy as np
     from scipy.optimize import nnls
@@ -113,6 +130,6 @@ def fit(times, sm_count=152):
                    key=lambda t: t[1])[0]
         losses.append(pick[3] / best - 1.0)
     names = ["t_iter_pair", "t_iter_128x256", "t_iter_128x128", "t_piece", "t_split", "t_part",
-             "t_launch", "t_dp_wave"]
+             "t_launch", "t_dp_wave", "t_split_shared", "t_part_shared"]
     return dict(zip(names, (round(float(c), 4) for c in coef))), \
         {"mean_loss": float(np.mean(losses)), "max_loss": float(np.max(losses))}

@@ -210,7 +210,7 @@ def test_plan_fields_follow_the_schedule_rules(lib):
 
 def test_auto_mode_picks_a_concrete_plan_from_the_cost_model():
     # choices of the fitted GB300 cost model on shapes of its calibration set (152 SMs)
-    cases = {(8192, 8192, 8192): (2, 2), (64, 14336, 4096): (1, 1), (512, 512, 32768): (1, 2),
+    cases = {(8192, 8192, 8192): (2, 2), (64, 14336, 4096): (1, 1), (512, 512, 32768): (2, 2),
              (1536, 1536, 1536): (1, 1), (16384, 2048, 2048): (2, 1), (2304, 2304, 8192): (2, 2)}
     for (M, N, K), (ctas_per_tile, mode) in cases.items():
         p = sk.sk_plan(0, M, N, K, 0, "auto", 152)
@@ -418,7 +418,8 @@ def test_auto_cost_constants_are_the_fit_of_the_shipped_sweep():
     iters = [float(v) for v in m.group(1).split(",")]
     rest = [float(v) for v in m.group(2).rstrip("}").split(",")]
     assert iters == [coef["t_iter_pair"], coef["t_iter_128x256"], coef["t_iter_128x128"]]
-    assert rest == [coef["t_piece"], coef["t_split"], coef["t_part"], coef["t_launch"]]
+    assert rest == [coef["t_piece"], coef["t_split"], coef["t_part"], coef["t_launch"],
+                    coef["t_split_shared"], coef["t_part_shared"]]
     assert quality["mean_loss"] < 0.02 and quality["max_loss"] < 0.15
 
 
