@@ -303,6 +303,38 @@ __device__ __forceinline__ void add_bias_chunk(const Args& a, int64_t n0, float 
   }
 }
 
+// The bias of this lane's column in each of kChunks 32-column chunks from n0 (0 past N), read
+// when a piece starts so that no chunk's store waits for it.
+template <int kChunks>
+__device__ __forceinline__ void load_bias_lanes(const Args& a, int64_t n0, int lane,
+                                                float (&b)[kChunks]) {
+#pragma unroll
+  for (int ch = 0; ch < kChunks; ++ch) {
+    const int64_t n = n0 + ch * 32 + lane;
+    b[ch] = 0.0f;
+    if (a.bias != nullptr && n < a.N)
+      b[ch] = a.out_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.bias)[n])
+                         : static_cast<const float*>(a.bias)[n];
+  }
+}
+
+// b[i] for a loop index i, without indexing the array in local memory.
+template <int kChunks>
+__device__ __forceinline__ float pick_chunk(const float (&b)[kChunks], int i) {
+  float r = b[kChunks - 1];
+#pragma unroll
+  for (int k = kChunks - 2; k >= 0; --k) r = i == k ? b[k] : r;
+  return r;
+}
+
+// v[j] += the bias of column j of the chunk, held by lane j.  (Nothing is added without a
+// bias, so that a zero keeps its sign.)
+__device__ __forceinline__ void add_bias_lanes(const Args& a, float (&v)[32], float b) {
+  if (a.bias == nullptr) return;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xffffffffu, b, j);
+}
+
 // Stages one piece of C -- 32 rows (one per lane) x 64 bytes -- in `buf` and writes it with a
 // TMA store at column x, row y.  The tensor map clips rows and columns past the matrix edge;
 // a piece that starts past the edge is skipped (returns false).  The caller alternates between
@@ -724,6 +756,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ? (lane < 16 ? static_cast<int64_t>(tm) * kBM + quarter * 16 + lane : args.M)
                             : y_warp + lane;
       const int64_t n_tile = static_cast<int64_t>(tn) * kBN;
+      float bias_l[kBN / 32];
+      load_bias_lanes(args, n_tile, lane, bias_l);
       bool has_next;
       {
         Cursor peek = cur;
@@ -854,10 +888,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (n_rem > 1) load_partial8(pq, rem + 8 * kBM + kSlot4, kBM);
             }
           }
+          add_bias_lanes(args, v, pick_chunk(bias_l, ch));
           if (args.c_tma && Cf::kMmaM == kBM) {   // (M = 64 accumulators: direct stores)
-            store_chunk_tma(args, &tmC, my_stage, sbuf, lane, n_tile + ch * 32, y_warp, v);
+            store_chunk_tma<false>(args, &tmC, my_stage, sbuf, lane, n_tile + ch * 32, y_warp, v);
           } else {
-            store_row_chunk(args, m, n_tile + ch * 32, v);
+            store_row_chunk<false>(args, m, n_tile + ch * 32, v);
           }
         }
       }

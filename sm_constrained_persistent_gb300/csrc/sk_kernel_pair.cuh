@@ -52,33 +52,6 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 
-// The bias of this lane's column in each of the four 32-column chunks of a warp's 128 columns
-// from n_half (0 past N), read when a piece starts so that no chunk's drain waits for it.
-__device__ __forceinline__ void load_bias_lanes(const Args& a, int64_t n_half, int lane,
-                                                float (&b)[4]) {
-#pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
-    const int64_t n = n_half + ch * 32 + lane;
-    b[ch] = 0.0f;
-    if (a.bias != nullptr && n < a.N)
-      b[ch] = a.out_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.bias)[n])
-                         : static_cast<const float*>(a.bias)[n];
-  }
-}
-
-// b[i] for a loop index i, without indexing the array in local memory.
-__device__ __forceinline__ float pick4(const float (&b)[4], int i) {
-  return i == 0 ? b[0] : i == 1 ? b[1] : i == 2 ? b[2] : b[3];
-}
-
-// v[j] += the bias of column j of the chunk, held by lane j.  (Nothing is added without a
-// bias, so that a zero keeps its sign as in the other kernels.)
-__device__ __forceinline__ void add_bias_lanes(const Args& a, float (&v)[32], float b) {
-  if (a.bias == nullptr) return;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xffffffffu, b, j);
-}
-
 // Address of the same shared-memory location in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
   uint32_t out;
@@ -731,7 +704,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
               if (s + 1 < n_src) add_partial8(w, pq, false);
             }
             if (next < 4 && n_src > 0) load_partial8(pp, src(0, next), kBM);
-            add_bias_lanes(args, w, pick4(bias_l, ch));
+            add_bias_lanes(args, w, pick_chunk(bias_l, ch));
             if constexpr (Cf::kTmaStore) {
               store_chunk_tma<false>(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else if (args.c_tma) {
@@ -800,7 +773,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
           if (store) {
             // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8);
             // MXFP4 ones when N allows
-            add_bias_lanes(args, w, pick4(bias_l, ch));
+            add_bias_lanes(args, w, pick_chunk(bias_l, ch));
             if constexpr (Cf::kTmaStore) {
               store_chunk_tma<false>(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else if (args.c_tma) {
@@ -848,7 +821,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
             }
             // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8);
             // MXFP4 ones when N allows
-            add_bias_lanes(args, w, pick4(bias_l, ch));
+            add_bias_lanes(args, w, pick_chunk(bias_l, ch));
             if constexpr (Cf::kTmaStore) {
               store_chunk_tma<false>(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else if (args.c_tma) {
@@ -916,7 +889,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<kMx>(),
             float(&w)[32] = *reinterpret_cast<float(*)[32]>(&v[ch * 32]);
             // bf16 and fp8 pairs always have 16-byte aligned rows of C (N is a multiple of 8);
             // MXFP4 ones when N allows
-            add_bias_lanes(args, w, pick4(bias_l, ch));
+            add_bias_lanes(args, w, pick_chunk(bias_l, ch));
             if constexpr (Cf::kTmaStore) {
               store_chunk_tma<false>(args, &tmC, my_stage, sbuf, lane, n_half + ch * 32, y_warp, w);
             } else if (args.c_tma) {
