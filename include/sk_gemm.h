@@ -96,7 +96,9 @@ typedef enum {
  *   bias: NULL, or N values of out_dtype.  Added once per output element, after all partial
  *      tiles are summed, broadcast over rows (tritonBLAS PR #67, Technical Details).
  *   C: row-major M x N of out_dtype (SK_BF16: rounded to nearest-even from fp32; SK_F32).
- *   M, N, K >= 1 and < 2^31.
+ *   M, N, K >= 1 and < 2^31.  Stream-K and hybrid calls whose Stream-K region holds 2^31 or
+ *      more tile k-iterations (products of 2^51 multiply-adds and up, on 128 x 128 tiles) are
+ *      refused with SK_ERR_UNSUPPORTED; persistent and data-parallel calls are not.
  *   num_sms: <= 0 means every SM; larger than the SM count is capped to it.  Ignored by
  *      SK_MODE_DP (grid = number of tiles).
  * Returns SK_OK once the kernel is queued on `stream`.

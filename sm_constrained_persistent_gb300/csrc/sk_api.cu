@@ -132,6 +132,9 @@ sk_status_t make_plan(int format, int64_t M, int64_t N, int64_t K, int num_sms, 
       break;
     }
   }
+  // The kernels' schedule arithmetic runs in 32 bits: a Stream-K region of 2^31 or more
+  // k-iterations (a product of 2^51 multiply-adds and up on 128 x 128 tiles) is refused.
+  if (sk_tiles * iters > kMaxDim) return SK_ERR_UNSUPPORTED;
   p->grid = static_cast<int32_t>(grid);
   p->whole_tiles = tiles - sk_tiles;
   p->sk_tiles = sk_tiles;

@@ -54,6 +54,26 @@ struct Unit {
   int32_t role;
 };
 
+// a / b and a % b for the values of a plan, all non-negative and below 2^31 (the planner refuses
+// larger Stream-K regions, and tiles are fewer).  On the GPU a 64-bit division is a long
+// software sequence; the 32-bit one is several times cheaper, which matters for the set-up of
+// every piece (a piece's first loads wait for it).
+__host__ __device__ __forceinline__ int64_t sk_div(int64_t a, int64_t b) {
+#ifdef __CUDA_ARCH__
+  return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+#else
+  return a / b;
+#endif
+}
+
+__host__ __device__ __forceinline__ int64_t sk_mod(int64_t a, int64_t b) {
+#ifdef __CUDA_ARCH__
+  return static_cast<int64_t>(static_cast<uint32_t>(a) % static_cast<uint32_t>(b));
+#else
+  return a % b;
+#endif
+}
+
 __host__ __device__ __forceinline__ int64_t sk_range_begin(const Plan& p, int64_t cta) {
   return cta * p.sk_base + (cta < p.sk_extra ? cta : p.sk_extra);
 }
@@ -65,8 +85,8 @@ __host__ __device__ __forceinline__ int64_t sk_range_len(const Plan& p, int64_t 
 // The CTA whose range holds Stream-K region iteration x.
 __host__ __device__ __forceinline__ int64_t sk_range_cta(const Plan& p, int64_t x) {
   const int64_t long_span = p.sk_extra * (p.sk_base + 1);  // iterations of the longer ranges
-  if (x < long_span) return x / (p.sk_base + 1);
-  return p.sk_base > 0 ? p.sk_extra + (x - long_span) / p.sk_base : p.sk_extra;
+  if (x < long_span) return sk_div(x, p.sk_base + 1);
+  return p.sk_base > 0 ? p.sk_extra + sk_div(x - long_span, p.sk_base) : p.sk_extra;
 }
 
 // The CTAs that continue the shared tile CTA `owner` owns, whose own piece is the tile's first
@@ -113,8 +133,8 @@ struct Cursor {
   __host__ __device__ __forceinline__ Cursor(const Plan& p, int64_t cta) {
     begin = sk_range_begin(p, cta);
     end = begin + sk_range_len(p, cta);
-    const int64_t first_full = (begin + p.iters - 1) / p.iters;   // first tile starting in range
-    const int64_t last_full = end / p.iters;                      // tiles ending in range
+    const int64_t first_full = sk_div(begin + p.iters - 1, p.iters);   // first tile starting in range
+    const int64_t last_full = sk_div(end, p.iters);                    // tiles ending in range
     full_next = first_full;
     full_end = last_full > first_full ? last_full : first_full;
     next_whole = cta;
@@ -135,8 +155,8 @@ struct Cursor {
     }
     if (step == 1) {
       step = 2;
-      if (begin < end && begin % p.iters != 0) {   // starts inside a tile: a contribution
-        const int64_t t = begin / p.iters;
+      if (begin < end && sk_mod(begin, p.iters) != 0) {   // starts inside a tile: a contribution
+        const int64_t t = sk_div(begin, p.iters);
         const int64_t tile_end = (t + 1) * p.iters;
         u.tile = p.whole_tiles + t;
         u.k0 = static_cast<int32_t>(begin - t * p.iters);
@@ -148,8 +168,8 @@ struct Cursor {
     if (step == 2) {
       step = 3;
       // ends inside a tile whose k = 0 lies in this range: the shared tile this CTA owns
-      const int64_t t = end / p.iters;
-      if (begin < end && end % p.iters != 0 && t * p.iters >= begin) {
+      const int64_t t = sk_div(end, p.iters);
+      if (begin < end && sk_mod(end, p.iters) != 0 && t * p.iters >= begin) {
         u.tile = p.whole_tiles + t;
         u.k0 = 0;
         u.k1 = static_cast<int32_t>(end - t * p.iters);
@@ -185,9 +205,9 @@ __host__ __device__ __forceinline__ int64_t raster_position(const Plan& p, int64
   const int64_t local = t - p.whole_tiles;
   const int64_t c = sk_range_cta(p, local * p.iters);      // owner: holds the tile's k = 0
   const int64_t start = sk_range_begin(p, c);
-  const int64_t first_owned = (start + p.iters - 1) / p.iters;   // first tile whose k = 0 is c's
+  const int64_t first_owned = sk_div(start + p.iters - 1, p.iters);   // first tile whose k = 0 is c's
   const int64_t tau = local - first_owned;
-  const int64_t f = p.sk_base / p.iters;   // every CTA owns f or f + 1 tiles
+  const int64_t f = sk_div(p.sk_base, p.iters);   // every CTA owns f or f + 1 tiles
   const int64_t pos = (tau < f) ? tau * p.grid + c : f * p.grid + (first_owned - c * f);
   return p.whole_tiles + pos;
 }
@@ -196,13 +216,13 @@ __host__ __device__ __forceinline__ void tile_coords(const Plan& p, int64_t t, i
                                                      int32_t& tn) {
   const int64_t r_pos = raster_position(p, t);
   const int64_t per_group = static_cast<int64_t>(p.group_m) * p.tiles_n;
-  const int64_t group = r_pos / per_group;
+  const int64_t group = sk_div(r_pos, per_group);
   const int64_t first_m = group * p.group_m;
   const int64_t rows_here =
       (p.tiles_m - first_m < p.group_m) ? (p.tiles_m - first_m) : p.group_m;
   const int64_t r = r_pos - group * per_group;
-  tm = static_cast<int32_t>(first_m + r % rows_here);
-  tn = static_cast<int32_t>(r / rows_here);
+  tm = static_cast<int32_t>(first_m + sk_mod(r, rows_here));
+  tn = static_cast<int32_t>(sk_div(r, rows_here));
 }
 
 }  // namespace sk

@@ -409,6 +409,25 @@ def test_streamk_256_cube_split_matches_golden(lib):
     assert np.array_equal(got[:, :5], want)
 
 
+def test_streamk_regions_of_2_31_iterations_are_refused():
+    # the kernels' schedule arithmetic runs in 32 bits: a Stream-K region of 2^31 or more tile
+    # k-iterations is refused; persistent plans of the same problem and the automatic choice
+    # (which skips refused candidates) stay available
+    big, tiles = (131072, 131072, 131072), {"tile_m": 128, "tile_n": 128}
+    for mode in ("streamk", "hybrid"):
+        with pytest.raises(sk.SkError) as e:
+            sk.sk_plan(0, *big, 0, mode, 152, dict(tiles, hybrid_sk_waves=10 ** 6))
+        assert e.value.status == sk.SK_ERR_UNSUPPORTED
+    p = sk.sk_plan(0, *big, 0, "persistent", 152, tiles)
+    assert p.tiles == 1024 * 1024
+    p = sk.sk_plan(0, *big, 0, "auto", 152)
+    assert p.sk_tiles * p.iters < 2 ** 31
+    p = sk.sk_plan(0, 65536, 65536, 512000, 0, "streamk", 152, tiles)   # just below the limit
+    assert p.sk_tiles * p.iters == 262144 * 8000 < 2 ** 31 and p.mode == 2
+    with pytest.raises(sk.SkError):                                       # at it: 2^18 x 2^13
+        sk.sk_plan(0, 65536, 65536, 524288, 0, "streamk", 152, tiles)
+
+
 def test_auto_cost_constants_are_the_fit_of_the_shipped_sweep():
     pytest.importorskip("scipy")
     from sm_constrained_persistent_gb300 import tuning
