@@ -133,3 +133,36 @@ def fit(times, sm_count=152):
              "t_launch", "t_dp_wave", "t_split_shared", "t_part_shared"]
     return dict(zip(names, (round(float(c), 4) for c in coef))), \
         {"mean_loss": float(np.mean(losses)), "max_loss": float(np.max(losses))}
+
+
+# The per-iteration scales of the estimate that are not fitted: MXFP4 and 96-wide k-iterations
+# against bf16 ones, and a tall (128-K) stage against two 64-K ones.
+MX_ITER_SCALE = 1.45
+N96_ITER_SCALE = 0.94
+TALL_ITER_SCALE = 0.97
+
+
+def plan_cost(p, coef, format=0):
+    """The automatic choice's estimate (us) of a plan `p` (an sk_plan_t) under the fitted
+    constants `coef` (fit()'s first result): the cost the library minimises over its candidates."""
+    kind = 0 if p.ctas_per_tile == 2 else (1 if p.tile_n == 256 else 2)
+    t_iter = [coef["t_iter_pair"], coef["t_iter_128x256"], coef["t_iter_128x128"]][kind]
+    t_iter *= MX_ITER_SCALE if format == 1 else 1.0
+    t_iter *= N96_ITER_SCALE if p.tile_n == 96 else 1.0
+    t_iter *= 2.0 * TALL_ITER_SCALE if format == 0 and p.tile_k == 128 else 1.0
+    g, T, I = max(p.grid, 1), p.tiles, p.iters
+    fixup = 0.0
+    if p.mode in (0, 1):
+        waves = math.ceil(T / g)
+        iters, pieces = waves * I, waves
+    else:
+        skT, whole = p.sk_tiles, p.whole_tiles
+        per = math.ceil(skT * I / g) if skT else 0
+        iters = per + math.ceil(whole / g) * I
+        pieces = math.ceil(whole / g) + (math.ceil(per / I) + 1 if skT else 0)
+        if skT:
+            split = per % I != 0 or (skT * I) % g != 0
+            shared = shared_finish(p, format)
+            fixup = ((coef["t_split_shared"] if shared else coef["t_split"]) if split else 0.0) + \
+                (coef["t_part_shared"] if shared else coef["t_part"]) * math.ceil(I / max(per, 1))
+    return coef["t_launch"] + iters * t_iter + pieces * coef["t_piece"] + fixup

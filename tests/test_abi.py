@@ -442,6 +442,41 @@ def test_auto_cost_constants_are_the_fit_of_the_shipped_sweep():
     assert quality["mean_loss"] < 0.02 and quality["max_loss"] < 0.15
 
 
+def test_auto_choice_is_the_cheapest_candidate_of_the_documented_estimate():
+    # tuning.plan_cost restates the estimate; the library's automatic plan must be its first
+    # cheapest candidate (tiles 256x256, 128x256, 128x128, 128x96 in that order, each under
+    # persistent, Stream-K and hybrid, with the planner's rules for one row of tiles)
+    pytest.importorskip("scipy")
+    from sm_constrained_persistent_gb300 import tuning
+    coef, _ = tuning.fit(tuning.load())
+    tiles = [(256, 256), (128, 256), (128, 128), (128, 96)]
+    shapes = [(8192, 8192, 8192), (1920, 1920, 16384), (512, 512, 16384), (64, 14336, 4096),
+              (96, 8192, 8192), (3000, 1000, 7000), (256, 4096, 4096), (1024, 2048, 8192),
+              (4096, 4096, 1024), (640, 2560, 16384), (1, 4096, 4096), (7168, 7168, 1536)]
+    for fmt in (0, 1, 2):
+        for (M, N, K) in shapes:
+            if fmt == 1 and (K % 32 or N % 2):
+                continue
+            best = None
+            for tm, tn in tiles:
+                if M <= 128 and (tm, tn) in ((128, 256), (256, 256)):
+                    continue
+                if tn == 96 and (fmt != 0 or M > 128):
+                    continue
+                for mode in ("persistent", "streamk", "hybrid"):
+                    try:
+                        p = sk.sk_plan(fmt, M, N, K, 0, mode, 152, {"tile_m": tm, "tile_n": tn})
+                    except sk.SkError:
+                        continue
+                    c = tuning.plan_cost(p, coef, fmt)
+                    if best is None or c < best[0]:
+                        best = (c, p)
+            auto = sk.sk_plan(fmt, M, N, K, 0, "auto", 152)
+            want = best[1]
+            assert (auto.mode, auto.tile_m, auto.tile_n, auto.grid) == \
+                (want.mode, want.tile_m, want.tile_n, want.grid), (fmt, M, N, K)
+
+
 def test_tensor_pipe_probes_compile_for_sm103a():
     """The measurement programs behind the kernels' MMA-kind and scale-copy choices build."""
     import shutil
