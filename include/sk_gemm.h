@@ -80,8 +80,9 @@ typedef enum { SK_F32 = 0, SK_BF16 = 1 } sk_dtype_t;
 typedef enum {
   SK_OK = 0,
   SK_ERR_INVALID_ARG = 1,     /* bad size, null or misaligned pointer, bad enum value      */
-  SK_ERR_UNSUPPORTED = 2,     /* valid request this build cannot run (e.g. no sm_103 GPU,  */
-                              /* or workspace too small while the stream is capturing)     */
+  SK_ERR_UNSUPPORTED = 2,     /* valid request the library cannot run (e.g. no sm_103 GPU, */
+                              /* a workspace too small while the stream is capturing, or a */
+                              /* Stream-K region of 2^31 tile k-iterations or more)        */
   SK_ERR_OOM = 3,             /* workspace allocation failed                               */
   SK_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed                         */
   SK_ERR_TIMEOUT = 5,         /* kernel-side: a bounded wait ran out (see sk_stream_status) */
