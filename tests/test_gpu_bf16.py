@@ -425,11 +425,12 @@ def test_tiles_finished_by_several_pairs_are_bit_exact(shape, num_sms, parties, 
         assert np.array_equal(gu.host_bits(c), want_bits)
 
 
-def test_tiles_finished_by_several_pairs_random_inputs_match_oracle():
-    p = inputs.bf16_problem(512, 512, 8192, seed=31, operand_scale="sqrt_k", bias="bf16_uniform")
-    c = gu.run_bf16(p, out="bf16", mode="streamk", num_sms=38, options=TILES["pair256"])
-    ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), "bf16")
-    gu.assert_close(gu.host_values(c), ref, "bf16")
+@pytest.mark.parametrize("bias,out", [("bf16_uniform", "bf16"), ("none", "bf16"), ("f32_normal", "f32")])
+def test_tiles_finished_by_several_pairs_random_inputs_match_oracle(bias, out):
+    p = inputs.bf16_problem(512, 512, 8192, seed=31, operand_scale="sqrt_k", bias=bias)
+    c = gu.run_bf16(p, out=out, mode="streamk", num_sms=38, options=TILES["pair256"])
+    ref = gu.reference(oracle.addmm_bf16(p["A"], p["B"], p["bias"]), out)
+    gu.assert_close(gu.host_values(c), ref, out)
 
 
 @pytest.mark.parametrize("dropped", ["finisher", "owner"])
