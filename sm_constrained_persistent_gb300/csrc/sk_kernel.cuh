@@ -812,22 +812,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // contributors 0 .. n_rem-1 (the nearest) are read by the drain
       const int n_rem = flag_status == kUnitStore ? n_contrib - n_staged : 0;
-      if (et == 0) {
+      if (et < 32) {
+        // Lane 0 of the first epilogue warp waits for the accumulator; an owner then waits for
+        // its remaining contributors' flags, lane l for contributors l, l + 32, ... side by side.
         uint32_t status = kUnitStore;
-        if (!wait_bar(&tfull[acc], acc_phase, abort_flag, args, kSiteEpilogue)) {
+        if (et == 0 && !wait_bar(&tfull[acc], acc_phase, abort_flag, args, kSiteEpilogue))
           status = kUnitAbort;
-        } else if (u.role == kRoleOwner) {
-          for (int c = 0; c < n_rem; ++c) {
+        status = __shfl_sync(0xffffffffu, status, 0);
+        if (status == kUnitStore && u.role == kRoleOwner) {
+          bool ok = true;
+          for (int c = et; c < n_rem && ok; c += 32) {
             uint32_t* f = args.flags + cta + 1 + c;
-            if (!wait_flag(f, args.epoch, args.timeout_ns)) {
-              record_error(args, kSiteFlag, u.tile);
-              status = kUnitSkip;
-              break;
-            }
-            *reinterpret_cast<volatile uint32_t*>(f) = 0u;  // consumed: ready for the next launch
+            ok = wait_flag(f, args.epoch, args.timeout_ns);
+            if (ok) *reinterpret_cast<volatile uint32_t*>(f) = 0u;  // consumed: ready for the next launch
+          }
+          if (!__all_sync(0xffffffffu, ok)) {
+            if (et == 0) record_error(args, kSiteFlag, u.tile);
+            status = kUnitSkip;
           }
         }
-        unit_status[acc] = status;
+        if (et == 0) unit_status[acc] = status;
       }
       named_barrier_sync(1, kEpilogueThreads);
       const uint32_t status = unit_status[acc];
