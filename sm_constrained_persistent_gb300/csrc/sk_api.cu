@@ -1044,6 +1044,10 @@ sk_status_t sk_autotune(int format, const void* A, const void* A_scale, const vo
   for (const Cand& c : cands) {
     sk_status_t st = run(c);                       // warm-up; refuses invalid combinations
     if (st == SK_ERR_INVALID_ARG || st == SK_ERR_NOT_CORESIDENT) continue;
+    if (st == SK_ERR_UNSUPPORTED) {   // e.g. a Stream-K region too large: other candidates may run
+      if (pick == nullptr) result = st;
+      continue;
+    }
     if (st != SK_OK) {
       result = st;
       pick = nullptr;
