@@ -3,8 +3,9 @@ benchmark names, against the oracle computed once per workload on all host threa
 
 Workloads (the seeded synthetic inputs of the benchmark): the bf16, MXFP4 and fp8 8192^3 addmm
 (bf16 bias, bf16 output), the wave-quantised 1920 x 1920 x 16384 GEMM (with its stated
-128 x 128 tiles and with the library's own tiles), and the SM-constrained persistent sweep over
-num_sms in {1, 16, 32, 64, 128, all} on 4096^3 and on the skinny 64 x 14336 x 4096.  Each case
+128 x 128 tiles and with the library's own tiles), the SM-constrained persistent sweep over
+num_sms in {1, 16, 32, 64, 128, all} on 4096^3 and on the skinny 64 x 14336 x 4096, and the
+few-tile, long-K 1024 x 1024 x 16384 GEMM whose split tiles several SM pairs finish together.  Each case
 compares all M x N outputs at the parity tolerance (bf16 output: |C - ref| <= 1e-2 + 1e-2 |ref|)
 and reports its worst element relative to the bound in the test summary."""
 import functools
@@ -93,3 +94,9 @@ def test_num_sms_sweep_every_element(cuda_device, parity_report, name, num_sms):
 @pytest.mark.parametrize("name", ["gemm_bf16_4096", "gemm_bf16_skinny_64x14336x4096"])
 def test_sweep_shapes_streamk_every_element(cuda_device, parity_report, name):
     _check_all(name, f"{name}/streamk", "streamk", parity_report)
+
+
+@pytest.mark.parametrize("mode", ["streamk", "hybrid", "dp"])
+def test_few_tiles_long_k_1024_every_element(cuda_device, parity_report, mode):
+    # 16 pair tiles on 76 pairs: ~5 pairs per tile, four of which finish it with its owner
+    _check_all("gemm_bf16_1024x1024x16384", f"1024x1024x16384/{mode}", mode, parity_report)
