@@ -107,9 +107,8 @@ __device__ __forceinline__ void mma(uint32_t d, uint64_t ad, uint64_t bd, uint32
 }
 
 // out[cta] = clocks, out[256 + cta] = nanoseconds of `iters` x 4 MMAs (issuing CTAs only).
-template <int kKind, bool kPair, int N>
+template <int kKind, bool kPair, int N, int M>
 __device__ void body(int iters, int random, unsigned long long* out) {
-  constexpr int M = kPair ? 256 : 128;
   extern __shared__ uint8_t raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 65536);
@@ -182,23 +181,24 @@ __device__ void body(int iters, int random, unsigned long long* out) {
   }
 }
 
-template <int kKind, int N>
+template <int kKind, int N, int M>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
     rate_pair(int iters, int random, unsigned long long* out) {
-  body<kKind, true, N>(iters, random, out);
+  body<kKind, true, N, M>(iters, random, out);
 }
 
-template <int kKind, int N>
+template <int kKind, int N, int M>
 __global__ void __launch_bounds__(128, 1) rate_single(int iters, int random, unsigned long long* out) {
-  body<kKind, false, N>(iters, random, out);
+  body<kKind, false, N, M>(iters, random, out);
 }
 
-template <int kKind, bool kPair, int N>
+// M: rows of one MMA (256 or 128 for a pair, 128 or 64 for one CTA); the operands are read
+// from the same 64 KB of shared memory whatever the shape.
+template <int kKind, bool kPair, int N, int M = (kPair ? 256 : 128)>
 bool run(const char* name, int sms, unsigned long long* d_out, int iters, int random) {
-  constexpr int M = kPair ? 256 : 128;
   constexpr int K = kKind == kF16 ? 16 : (kKind == kF8 ? 32 : 64);
   const size_t smem = 200 * 1024;   // one CTA per SM
-  auto* fn = kPair ? rate_pair<kKind, N> : rate_single<kKind, N>;
+  auto* fn = kPair ? rate_pair<kKind, N, M> : rate_single<kKind, N, M>;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return false;
@@ -247,6 +247,12 @@ int main() {
   ok &= run<kMxf4, true, 128>("kind::mxf4.block_scale.scale_vec::2X", sms, d_out, iters, 0);
   ok &= run<kF16, false, 256>("kind::f16", sms, d_out, iters, 0);
   ok &= run<kMxf4, false, 256>("kind::mxf4.block_scale.scale_vec::2X", sms, d_out, iters, 0);
+  // smaller bf16 shapes, as a ragged edge tile could issue them
+  ok &= run<kF16, true, 128>("kind::f16", sms, d_out, iters, 0);
+  ok &= run<kF16, true, 256, 128>("kind::f16", sms, d_out, iters, 0);
+  ok &= run<kF16, true, 128, 128>("kind::f16", sms, d_out, iters, 0);
+  ok &= run<kF16, false, 128>("kind::f16", sms, d_out, iters, 0);
+  ok &= run<kF16, false, 256, 64>("kind::f16", sms, d_out, iters, 0);
   cudaFree(d_out);
   return ok ? 0 : 1;
 }
