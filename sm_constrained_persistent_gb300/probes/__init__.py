@@ -8,7 +8,8 @@ for sm_103a (built with nvcc into ``probes/_build``):
   handshake, scale-factor copies into tensor memory) added to back-to-back MMAs one at a time.
 * ``tma_stream``: the read rate of a 4096 x 14336 bf16 matrix (the B operand of the skinny
   64 x 14336 x 4096 GEMM) streamed through TMA in column strips, per strip width, box shape,
-  ring depth, K split and L2 promotion, with nothing else running.
+  ring depth, K split and L2 promotion, with nothing else running, and with each stage held for
+  an MMA's time before it is handed back.
 * ``host_link``: host <-> device rates between pinned host memory and the GPU for the host-buffer
   entry points (268 MB in, 134 MB out): copy engines on 1, 2 or 4 streams, and kernels that load
   or store pinned host memory directly, per grid size, each direction alone and both at once.

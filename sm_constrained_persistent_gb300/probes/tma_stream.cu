@@ -4,7 +4,8 @@
 // CTA (strip, part) reads columns [strip * W, (strip + 1) * W) of rows [part * K / P, (part +
 // 1) * K / P), H rows per stage, as W / box_cols boxes of box_cols x H, through a ring of S
 // stages in shared memory.  One thread issues the copies, another waits for each stage and hands
-// it back at once, so the only limit is how fast the bytes arrive.  Three copies of the matrix
+// it back at once (or, where a hold is given, that many nanoseconds after it lands, as an MMA
+// reading the stage would), so the only limit is how fast the bytes arrive.  Three copies of the matrix
 // (351 MB, well over the 129 MB L2) are read in turn by launches timed back to back, so every
 // launch reads from DRAM and the event timer's ~2 us resolution is spread over six launches.
 // Each line of output is one pattern: its parameters, the CTAs it runs, the time per launch and
@@ -64,7 +65,7 @@ __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
 
 __global__ void __launch_bounds__(64, 1)
     stream_kernel(const __grid_constant__ CUtensorMap tm, int strip_cols, int box_cols, int box_h,
-                  int stages, int parts, uint32_t* err) {
+                  int stages, int parts, int hold_ns, uint32_t* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -121,6 +122,11 @@ __global__ void __launch_bounds__(64, 1)
         atomicExch(err, 2u);
         break;
       }
+      if (hold_ns > 0) {   // bounded: hold_ns is at most a few microseconds
+        const uint64_t h0 = now_ns();
+        while (now_ns() - h0 < static_cast<uint64_t>(hold_ns)) {
+        }
+      }
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&empty[s]))
                    : "memory");
     }
@@ -143,6 +149,7 @@ using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, voi
 struct Pattern {
   int strip_cols, box_cols, box_h, stages, parts;
   CUtensorMapL2promotion promo;
+  int hold_ns;   // the consumer's hold per stage (0: handed back at once)
 };
 
 }  // namespace
@@ -192,6 +199,11 @@ int main() {
       // narrow strips, many CTAs
       {64, 64, 64, 6, 1, P256},   {64, 64, 128, 3, 1, P256},  {64, 64, 256, 2, 1, P256},
       {32, 32, 64, 6, 1, P256},
+      // 96-wide strips in 128-row boxes with a 200 ns hold per stage, as the tall-stage kernel's
+      // MMAs take: how many stages hide it
+      {96, 32, 128, 5, 1, P256, 200}, {96, 32, 128, 6, 1, P256, 200}, {96, 32, 128, 7, 1, P256, 200},
+      {96, 32, 128, 8, 1, P256, 200}, {96, 32, 128, 5, 1, P256, 0},   {96, 32, 128, 7, 1, P256, 0},
+      {128, 64, 128, 4, 1, P256, 260}, {128, 64, 128, 6, 1, P256, 260},
   };
 
   cudaEvent_t e0, e1;
@@ -235,7 +247,7 @@ int main() {
       CHECK(cudaEventRecord(e0));
       for (int l = 0; l < kLaunches; ++l)
         stream_kernel<<<ctas, 64, smem>>>(tm[l % kCopies], p.strip_cols, p.box_cols, p.box_h,
-                                          p.stages, p.parts, err);
+                                          p.stages, p.parts, p.hold_ns, err);
       CHECK(cudaEventRecord(e1));
       CHECK(cudaEventSynchronize(e1));
       float ms = 0;
@@ -248,8 +260,8 @@ int main() {
     best = ts[ts.size() / 2];
     std::printf(
         "{\"strip_cols\": %d, \"box\": [%d, %d], \"stages\": %d, \"k_parts\": %d, \"l2_promo\": %d, "
-        "\"ctas\": %d, \"ctas_per_sm\": %d, \"us\": %.2f, \"GBs\": %.0f, \"err\": %u}\n",
-        p.strip_cols, p.box_cols, p.box_h, p.stages, p.parts, p.promo == P256 ? 256 : 0, ctas,
+        "\"hold_ns\": %d, \"ctas\": %d, \"ctas_per_sm\": %d, \"us\": %.2f, \"GBs\": %.0f, \"err\": %u}\n",
+        p.strip_cols, p.box_cols, p.box_h, p.stages, p.parts, p.promo == P256 ? 256 : 0, p.hold_ns, ctas,
         per_sm, best * 1000.0f, bytes / (best * 1e-3) / 1e9, h_err);
     std::fflush(stdout);
     if (h_err != 0) return 2;
