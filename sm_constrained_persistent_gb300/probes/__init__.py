@@ -1,4 +1,4 @@
-"""Tensor-pipe measurements behind the kernels' design choices, as two standalone CUDA programs
+"""Measurements behind the kernels' design choices, as standalone CUDA programs for sm_103a
 for sm_103a (built with nvcc into ``probes/_build``):
 
 * ``tc_rate``: clocks per tcgen05.mma for each MMA kind the kernels use or could use (kind::f16,
@@ -14,6 +14,9 @@ for sm_103a (built with nvcc into ``probes/_build``):
   entry points (268 MB in, 134 MB out): copy engines on 1, 2 or 4 streams, and kernels that load
   or store pinned host memory directly, per grid size, each direction alone and both at once.
 
+* ``l2_reuse``: how much of a re-read working set (16-192 MB) the L2 still holds after one read, and
+  whether what one half of the SMs read is found in L2 by the other half.
+
 ``python -m sm_constrained_persistent_gb300.probes`` builds and runs them on cuda:0 and prints
 one JSON line per measurement.  Measurement only: nothing here is on the GEMM path.
 """
@@ -24,7 +27,7 @@ import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 BUILD = os.path.join(HERE, "_build")
-PROBES = ("tc_rate", "tc_pipeline", "tma_stream", "host_link")
+PROBES = ("tc_rate", "tc_pipeline", "tma_stream", "host_link", "l2_reuse")
 
 
 def build(name: str) -> str:
